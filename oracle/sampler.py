@@ -1,0 +1,323 @@
+"""Oracle: the lossless acceptance sampler of the verify step.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  float64 throughout.
+
+Sources, all restated here in plain steps:
+
+* "Speculative Decoding" (atlas), section "One round and shifted logits":
+  the drafter proposes gamma tokens with their actual proposal
+  probabilities; the target scores the block, giving gamma distributions that
+  check the proposals plus one distribution after the last proposal; checks
+  run left to right; the first rejection commits a corrected token and drops
+  every later proposal; if all survive a bonus target token is sampled.  Row
+  i of the target (row 0 = the pending anchor) checks draft i + 1: comparing
+  unshifted logits is an off-by-one error.
+* Same page, "Exact sampling: account for every probability" and the
+  one-position listing under "Implementation roadmap and tests": accept the
+  proposal x with probability min(1, p(x)/q(x)); on rejection draw from the
+  positive part of p - q, renormalised.
+* "Drafters and Speculative Decoding", section "Sampling needs a correction
+  rule" (three-token example) and "Greedy verification".
+* "Speculative Decoding" (atlas), "Greedy, sampling and the real sampler":
+  greedy accepts while the proposal equals the target argmax and emits the
+  argmax at the first mismatch; p and q must include temperature and
+  truncation as actually served.
+* Same page, "Chains, trees and visibility": a tree needs its own
+  proposal/sampling rule; the rule used here is described in tree_walk.
+
+Readings where the pages are silent (each also listed in the design notes):
+  * z = logits / T; top-k keeps the k largest z (ties: lower token id first);
+    top-p then keeps the shortest prefix, in (probability desc, id asc) order
+    of the top-k-renormalised distribution, whose mass reaches top_p,
+    including the crossing token; p is the softmax over the kept set.
+    T, top_p are taken at their fp32 values, as served.
+  * The acceptance test for u in [0, 1) is u * q(x) < p(x): the same event as
+    u < min(1, p/q), without a division.  q(x) = 0 < p(x) therefore accepts
+    and is reported; p(x) = 0 always rejects.
+  * A draw from a weight vector w takes the first token id t whose running
+    sum in ascending id order exceeds u * sum(w).  One uniform, u_final (the
+    last one of the sequence), serves the correction draw and the bonus draw.
+  * If the residual has zero mass after a rejection (possible only through
+    rounding), the draw uses p itself and the sequence is reported.
+  * Greedy takes the lowest id among equal maxima.
+  * With eos_id >= 0, emission stops after the first EOS token, whether it is
+    an accepted draft or the correction/bonus token.
+
+Decision flags: a sequence whose outcome sits within FLAG_EPS of a decision
+boundary is reported as flagged; bit-exact comparison skips flagged sequences.
+  * ratio test: |u - p(x)/q(x)| < FLAG_EPS;
+  * inverse-CDF draw: u * Z within FLAG_EPS * Z of the chosen token's edges;
+  * top-p: the cumulative mass at the cutoff (either side) within FLAG_EPS of top_p.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+
+FLAG_EPS = 1e-5
+
+# per-sequence report bits (match the library's status_per_seq bits)
+ST_QZERO = 1        # a proposed token had q(x) = 0
+ST_NONFINITE = 2    # NaN or +inf in a target logit row that was read
+ST_RESID_ZERO = 4   # residual mass was zero after a rejection
+
+
+@dataclass
+class SamplerCfg:
+    temperature: float = 1.0
+    top_k: int = 0
+    top_p: float = 1.0
+    greedy: bool = False
+    eos_id: int = -1
+
+
+def _f32(x) -> float:
+    return float(np.float32(x))
+
+
+def target_distribution(logits_row, cfg: SamplerCfg):
+    """p over the vocabulary for one target row.  Returns (p, flagged)."""
+    l = np.asarray(logits_row, dtype=np.float64)
+    V = l.shape[0]
+    if np.any(np.isnan(l)) or np.any(l == np.inf):
+        raise ValueError("non-finite target logit")
+    T = _f32(cfg.temperature)
+    top_p = _f32(cfg.top_p)
+    z = l / T
+    order = np.lexsort((np.arange(V), -z))          # z descending, then id ascending
+    kept = order
+    if 0 < cfg.top_k < V:
+        kept = kept[:cfg.top_k]
+    flagged = False
+    if 0.0 < top_p < 1.0:
+        zk = z[kept]
+        e = np.exp(zk - zk[0])
+        c = np.cumsum(e / e.sum())
+        reach = np.nonzero(c >= top_p)[0]
+        n = int(reach[0]) + 1 if reach.size else len(kept)
+        flagged = abs(c[n - 1] - top_p) < FLAG_EPS or (n >= 2 and abs(c[n - 2] - top_p) < FLAG_EPS)
+        kept = kept[:n]
+    p = np.zeros(V)
+    zk = z[kept]
+    e = np.exp(zk - zk.max())
+    p[kept] = e / e.sum()
+    return p, flagged
+
+
+def inverse_cdf(w, u):
+    """First id t (ascending) whose running sum of w exceeds u * sum(w).
+
+    Returns (t, flagged)."""
+    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    Z = c[-1]
+    if not Z > 0:
+        raise ValueError("draw from a zero-mass vector")
+    target = float(u) * Z
+    t = int(np.searchsorted(c, target, side="right"))
+    lo = c[t - 1] if t > 0 else 0.0
+    flagged = (target - lo) < FLAG_EPS * Z or (c[t] - target) < FLAG_EPS * Z
+    return t, bool(flagged)
+
+
+def residual(p, q):
+    """norm(max(0, p - q)) and its mass before normalising."""
+    w = np.maximum(0.0, np.asarray(p, np.float64) - np.asarray(q, np.float64))
+    m = w.sum()
+    return (w / m if m > 0 else w), m
+
+
+def _ratio_flag(u, px, qx) -> bool:
+    return qx > 0 and abs(float(u) - px / qx) < FLAG_EPS
+
+
+def chain_walk(p_rows, q_rows, drafts, u, eos_id=-1):
+    """Left-to-right verification of one chain, given the final distributions.
+
+    p_rows [R, V]: target distribution after block row i (row 0 = anchor).
+    q_rows [R-1, V]: q_rows[i] is the distribution that proposed drafts[i].
+    drafts [R-1]; u [R]: u[i] tests drafts[i], u[R-1] is the final draw.
+    Returns dict(accepted_len, emitted, flagged, status).
+    """
+    R = len(p_rows)
+    gamma = R - 1
+    emitted, flagged, status = [], False, 0
+    u_final = u[gamma]
+    for i in range(gamma):
+        x = int(drafts[i])
+        px, qx = float(p_rows[i][x]), float(q_rows[i][x])
+        if qx == 0.0:
+            status |= ST_QZERO
+        flagged |= _ratio_flag(u[i], px, qx)
+        if float(u[i]) * qx < px:                    # accept with prob min(1, p/q)
+            emitted.append(x)
+            if x == eos_id:
+                return dict(accepted_len=i + 1, emitted=emitted, flagged=flagged, status=status)
+            continue
+        w, mass = residual(p_rows[i], q_rows[i])     # first rejection: correction
+        if mass == 0.0:
+            w = p_rows[i]
+            status |= ST_RESID_ZERO
+            flagged = True
+        t, fl = inverse_cdf(w, u_final)
+        emitted.append(t)
+        return dict(accepted_len=i, emitted=emitted, flagged=flagged | fl, status=status)
+    t, fl = inverse_cdf(p_rows[gamma], u_final)      # every draft survived: bonus
+    emitted.append(t)
+    return dict(accepted_len=gamma, emitted=emitted, flagged=flagged | fl, status=status)
+
+
+def greedy_argmax(row) -> int:
+    """Lowest id among the maxima of one logit row."""
+    return int(np.argmax(np.asarray(row, np.float64)))
+
+
+def greedy_walk(logits, drafts, eos_id=-1):
+    R = len(logits)
+    gamma = R - 1
+    emitted = []
+    for i in range(gamma):
+        a = greedy_argmax(logits[i])
+        x = int(drafts[i])
+        if x == a:
+            emitted.append(x)
+            if x == eos_id:
+                return dict(accepted_len=i + 1, emitted=emitted, flagged=False, status=0)
+            continue
+        emitted.append(a)
+        return dict(accepted_len=i, emitted=emitted, flagged=False, status=0)
+    emitted.append(greedy_argmax(logits[gamma]))
+    return dict(accepted_len=gamma, emitted=emitted, flagged=False, status=0)
+
+
+def accept_chain(logits, q_rows, drafts, u, cfg: SamplerCfg):
+    """One sequence: logits [R,V] fp32 values, q_rows [R-1,V], drafts [R-1], u [R]."""
+    logits = np.asarray(logits)
+    if cfg.greedy or cfg.temperature == 0:
+        res = greedy_walk(logits, drafts, cfg.eos_id)
+        res["p"] = None
+        return res
+    p_rows, pflag = [], False
+    for i in range(len(logits)):
+        p, fl = target_distribution(logits[i], cfg)
+        p_rows.append(p)
+        pflag |= fl
+    res = chain_walk(p_rows, q_rows, drafts, u, cfg.eos_id)
+    res["flagged"] = res["flagged"] or pflag
+    res["p"] = np.stack(p_rows)
+    return res
+
+
+def tree_walk(p_nodes, q_nodes, tokens, parent, u, eos_id=-1):
+    """Draft-tree acceptance.  [READING: the pages give no rule]
+
+    The rule is the multi-candidate form of the classical one, for children
+    drawn i.i.d. from q at their parent: start at the anchor (node 0) with
+    p' = p_0.  Try the children of the current node v in storage order; child
+    c (token t) is accepted iff u[c-1] * q_v(t) < p'(t), and then the walk
+    moves to c with p' = p_c.  A rejected child replaces p' by
+    norm(max(0, p' - q_v)) before the next child is tried.  When no child is
+    accepted (or v is a leaf) the final token is drawn from p' with u[N-1].
+    For a chain (one child per node) this is exactly chain_walk.
+
+    p_nodes, q_nodes [N, V]; tokens [N] (node 0 unused); parent [N]; u [N].
+    Returns dict(accepted_len, path, emitted, flagged, status).
+    """
+    N = len(p_nodes)
+    v = 0
+    pcur = np.asarray(p_nodes[0], np.float64)
+    path, emitted, flagged, status = [], [], False, 0
+    children = [[c for c in range(N) if int(parent[c]) == v_] for v_ in range(N)]
+    while True:
+        moved = False
+        for c in children[v]:
+            t = int(tokens[c])
+            px, qx = float(pcur[t]), float(q_nodes[v][t])
+            if qx == 0.0:
+                status |= ST_QZERO
+            flagged |= _ratio_flag(u[c - 1], px, qx)
+            if float(u[c - 1]) * qx < px:
+                path.append(c)
+                emitted.append(t)
+                v = c
+                pcur = np.asarray(p_nodes[c], np.float64)
+                moved = True
+                break
+            w, mass = residual(pcur, q_nodes[v])
+            if mass == 0.0:
+                status |= ST_RESID_ZERO
+                flagged = True
+            else:
+                pcur = w
+        if moved and emitted[-1] == eos_id:
+            break
+        if not moved:
+            t, fl = inverse_cdf(pcur, u[N - 1])
+            emitted.append(t)
+            flagged |= fl
+            break
+    return dict(accepted_len=len(path), path=path, emitted=emitted, flagged=flagged,
+                status=status)
+
+
+def accept_tree(logits, q_nodes, tokens, parent, u, cfg: SamplerCfg):
+    logits = np.asarray(logits)
+    N = len(logits)
+    if cfg.greedy or cfg.temperature == 0:
+        # greedy on a tree: follow the first child equal to the target argmax
+        v, path, emitted = 0, [], []
+        while True:
+            a = greedy_argmax(logits[v])
+            nxt = [c for c in range(N) if int(parent[c]) == v and int(tokens[c]) == a]
+            emitted.append(a)
+            if not nxt or a == cfg.eos_id:
+                if nxt:
+                    path.append(nxt[0])
+                break
+            path.append(nxt[0])
+            v = nxt[0]
+        return dict(accepted_len=len(path), path=path, emitted=emitted, flagged=False,
+                    status=0, p=None)
+    p_nodes, pflag = [], False
+    for i in range(N):
+        p, fl = target_distribution(logits[i], cfg)
+        p_nodes.append(p)
+        pflag |= fl
+    res = tree_walk(p_nodes, q_nodes, tokens, parent, u, cfg.eos_id)
+    res["flagged"] = res["flagged"] or pflag
+    res["p"] = np.stack(p_nodes)
+    return res
+
+
+def _pad(rows, width):
+    out = np.full((len(rows), width), -1, dtype=np.int64)
+    for b, r in enumerate(rows):
+        out[b, :len(r)] = r
+    return out
+
+
+def accept_chain_batch(logits, q, drafts, u, cfg: SamplerCfg, want_p=False):
+    """Batch form: logits [B,R,V], q [B,R-1,V], drafts [B,R-1], u [B,R]."""
+    B, R = logits.shape[0], logits.shape[1]
+    res = [accept_chain(logits[b], None if q is None else q[b], drafts[b], u[b], cfg)
+           for b in range(B)]
+    out = dict(accepted_len=np.array([r["accepted_len"] for r in res]),
+               emitted=_pad([r["emitted"] for r in res], R),
+               flagged=np.array([r["flagged"] for r in res]),
+               status=np.array([r["status"] for r in res]))
+    if want_p and res and res[0]["p"] is not None:
+        out["p"] = np.stack([r["p"] for r in res])
+    return out
+
+
+def accept_tree_batch(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=False):
+    """Batch form: logits, q [B,N,V]; tokens, parent [B,N]; u [B,N]."""
+    B, N = logits.shape[0], logits.shape[1]
+    res = [accept_tree(logits[b], None if q is None else q[b], tokens[b], parent[b], u[b], cfg)
+           for b in range(B)]
+    out = dict(accepted_len=np.array([r["accepted_len"] for r in res]),
+               path=_pad([r["path"] for r in res], N),
+               emitted=_pad([r["emitted"] for r in res], N),
+               flagged=np.array([r["flagged"] for r in res]),
+               status=np.array([r["status"] for r in res]))
+    if want_p and res and res[0]["p"] is not None:
+        out["p"] = np.stack([r["p"] for r in res])
+    return out
