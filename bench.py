@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+tree visibility (spec_tree_prepare), split-K verify attention (partials +
+log-sum-exp combine) and the acceptance sampler.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Timing: inputs resident in HBM; the step is captured once in a CUDA graph
+and replayed; L2 is flushed (a 2 x L2-size write) before every timed step,
+outside the timed events; each step is timed with CUDA events on its stream;
+K steps are bracketed by a barrier + synchronize; the max over ranks is
+reported.  The dominant kernel (the split-K partial pass) is timed with its
+own events inside the captured step for the roofline entry.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle leg runs on one core
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_verification_76_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verified positions/sec and achieved HBM GB/s (fraction of roofline), 1×GB300"
+UNIT = "positions/s"
+DEFAULT_WORKLOAD = "llama8b_chain"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device="cpu") -> float:
+    """Largest value of x over all ranks (x itself when running alone)."""
+    if ws <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device="cpu") -> float:
+    if ws <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if k in d and isinstance(d[k], (int, float)):
+                return float(d[k]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_76_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the partial kernel from an ncu capture, if
+    the capture was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "attn_partial_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_sha") == source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the step on the GPU
+class GpuStep:
+    """All buffers of one verify step, resident on the device."""
+
+    def __init__(self, spec: wl.Spec, device, seed=None):
+        import speculative_decoding_verification_76_gb300 as sv
+        self.sv = sv
+        self.spec = spec
+        self.dev = device
+        w = wl.make_workload(spec, seed=seed, device=device)
+        self.w = w
+        B, R = spec.B, spec.R
+        self.anc = torch.empty((B, R), dtype=torch.int64, device=device)
+        self.pos = torch.empty((B, R), dtype=torch.int32, device=device)
+        self.tst = torch.empty((B,), dtype=torch.int32, device=device)
+        self.attn = sv.AttnCall(w.q, w.k_cache, w.v_cache, w.block_table, w.ctx_len, self.anc,
+                                num_splits=spec.num_splits)
+        self.cfg = sv.SamplerConfig(temperature=spec.temperature, top_k=spec.top_k,
+                                    top_p=spec.top_p, greedy=spec.greedy)
+        self.sws = sv.new_workspace(sv.sample_workspace_size(B, R, spec.V), device)
+        self.sout = dict(accepted_len=torch.empty(B, dtype=torch.int32, device=device),
+                         emitted=torch.empty((B, R), dtype=torch.int32, device=device),
+                         status=torch.empty(B, dtype=torch.int32, device=device))
+        if spec.is_tree:
+            self.sout["path"] = torch.empty((B, R), dtype=torch.int32, device=device)
+        self.ev = None
+        self.launches_per_step = 4
+
+    def run(self, ev=None):
+        sv, w = self.sv, self.w
+        sv.tree_prepare(w.parent, w.ctx_len, anc_mask=self.anc, pos_ids=self.pos, status=self.tst)
+        if ev is not None:
+            ev[0].record()
+        self.attn.partials()
+        if ev is not None:
+            ev[1].record()
+        self.attn.combine()
+        if self.spec.is_tree:
+            sv.accept_sample_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms,
+                                  self.cfg, workspace=self.sws, out=self.sout)
+        else:
+            sv.accept_sample(w.logits, None if self.spec.greedy else w.draft_probs,
+                             w.draft_tokens, w.uniforms, self.cfg, workspace=self.sws,
+                             out=self.sout)
+
+
+def bench_gpu(args, spec, ws, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_verification_76_gb300 as sv
+    sv.load()
+    step = GpuStep(spec, dev)
+    ctx = step.w.ctx_len.cpu().numpy()
+    nbytes = wl.algorithmic_bytes(spec, ctx)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(3):                     # eager warm-up: attributes, descriptors
+        step.run()
+    torch.cuda.synchronize()
+    try:   # events captured as graph nodes time the partial kernel inside each replay
+        ev_in = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    except TypeError:
+        ev_in = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run(ev_in)
+    torch.cuda.synchronize()
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, part_ms = [], []
+    with ClockSampler(gpu_index) as clk:
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        barrier(ws)
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            if ev_in is not None:
+                part_ms.append(ev_in[0].elapsed_time(ev_in[1]))
+        torch.cuda.synchronize()
+        barrier(ws)
+        if ev_in is None:   # no graph event nodes: time the partial pass eagerly
+            for _ in range(min(args.steps, 200)):
+                flush.zero_()
+                e0.record(stream)
+                step.attn.partials()
+                e1.record(stream)
+                e1.synchronize()
+                part_ms.append(e0.elapsed_time(e1))
+    clocks = clk.summary()
+    err = sv.workspace_error(step.attn.workspace) | sv.workspace_error(step.sws)
+    if err:
+        raise RuntimeError(f"device wait timed out (error word {err:#x})")
+
+    mean_ms = statistics.fmean(step_ms)
+    mean_ms_all = max_over_ranks(mean_ms, ws, device=dev)
+    positions = spec.B * spec.R
+    total_positions = sum_over_ranks(positions, ws, device=dev)
+    value = total_positions / (mean_ms_all * 1e-3)
+    part_mean = statistics.fmean(part_ms)
+    peak, peak_src = hbm_peak()
+    attn_gbs = nbytes["attn"] / (part_mean * 1e-3) / 1e9
+    step_gbs = nbytes["step"] / (mean_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(spec.name)
+
+    acc = step.sout["accepted_len"].cpu().numpy()
+    e2e = bench_e2e(step, spec, max(3, min(args.steps, 50)), ws, dev)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": spec.name, "global_batch": spec.B * ws, "seq_len": int(ctx.max()),
+            "rows_per_seq": spec.R, "tree": spec.is_tree, "q_heads": spec.Hq,
+            "kv_heads": spec.Hkv, "head_dim": spec.D, "vocab": spec.V, "page_size": spec.page_size,
+            "temperature": spec.temperature, "top_k": spec.top_k, "top_p": spec.top_p,
+            "greedy": spec.greedy, "num_splits": step.sv.attn_num_splits(
+                spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
+                step.w.block_table.shape[1], spec.num_splits),
+            "sampler_dtype": "f32", "parallelism": f"replicas{ws}",
+            "l2": "flushed before every timed step (2 x L2 write, outside the timed events)",
+            "timing": "CUDA-graph replay, CUDA events per step"},
+        "sequences_per_s": sum_over_ranks(spec.B, ws, device=dev) / (mean_ms_all * 1e-3),
+        "step_hbm_gbs": step_gbs, "step_hbm_frac": step_gbs / peak,
+        "step_algorithmic_bytes": nbytes["step"],
+        "roofline": {"bound": "hbm", "kernel": "attn_partial_bf16 (split-K partials)",
+                     "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": attn_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes": nbytes["attn"], "mean_launch_us": part_mean * 1e3,
+                     "peak_source": peak_src},
+        "accepted_len_hist": np.bincount(np.clip(acc, 0, None),
+                                         minlength=spec.R).tolist(),
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return out
+
+
+def bench_e2e(step: GpuStep, spec, n, ws, dev):
+    """Same metric through the public API with host buffers: every step
+    copies its inputs from pinned host memory, runs the three calls and reads
+    the accepted lengths and emitted tokens back."""
+    sv, w = step.sv, step.w
+    names = ["q", "block_table", "ctx_len", "parent", "logits", "draft_probs", "draft_tokens",
+             "uniforms"]
+    host = {k: getattr(w, k).cpu().pin_memory() for k in names}
+    dst = {k: torch.empty_like(getattr(w, k)) for k in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    res_host = {k: torch.empty_like(v, device="cpu").pin_memory()
+                for k, v in step.sout.items() if k in ("accepted_len", "emitted")}
+    d2h = sum(t.numel() * t.element_size() for t in res_host.values())
+    cfg = step.cfg
+
+    def one():
+        for k in names:
+            dst[k].copy_(host[k], non_blocking=True)
+        anc, _, _ = sv.tree_prepare(dst["parent"], dst["ctx_len"])
+        sv.verify_attn(dst["q"], w.k_cache, w.v_cache, dst["block_table"], dst["ctx_len"], anc,
+                       num_splits=spec.num_splits, workspace=step.attn.workspace)
+        if spec.is_tree:
+            r = sv.accept_sample_tree(dst["logits"], dst["draft_probs"], dst["draft_tokens"],
+                                      dst["parent"], dst["uniforms"], cfg, workspace=step.sws)
+        else:
+            r = sv.accept_sample(dst["logits"], None if spec.greedy else dst["draft_probs"],
+                                 dst["draft_tokens"], dst["uniforms"], cfg, workspace=step.sws)
+        for k in res_host:
+            res_host[k].copy_(r[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t0) / n
+    dt = max_over_ranks(dt, ws, device=dev)
+    return {"value": sum_over_ranks(spec.B * spec.R, ws, device=dev) / dt, "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": dt * 1e3, "steps": n,
+            "note": "KV cache resident in HBM; per-step inputs copied from pinned host memory"}
+
+
+# ------------------------------------------------------------------ the oracle on the host
+def cpu_inputs(spec, device=None):
+    """The workload's inputs on the host (generated where the GPU run makes them)."""
+    dev = device if device is not None else ("cuda" if torch.cuda.is_available() else "cpu")
+    w = wl.make_workload(spec, device=dev)
+    return w.to("cpu")
+
+
+def oracle_sample_plan(spec):
+    """A bounded sample of one step: every sampler row, and attention for a
+    subset of query heads (the step time is scaled up by Hq / heads)."""
+    heads = max(1, min(spec.Hq, 4 if spec.Hq >= 4 else spec.Hq))
+    batches = list(range(min(spec.B, 2)))
+    return heads, batches
+
+
+def oracle_step(spec, w, heads, batches):
+    """Time one bounded oracle step; returns estimated full-step seconds."""
+    import oracle
+    from oracle.sampler import SamplerCfg
+    from tests.util import oracle_attention   # plumbing: one sequence at a time
+    t0 = time.perf_counter()
+    anc, _, _ = oracle.tree.tree_prepare(w.parent.numpy(), w.ctx_len.numpy())
+    oracle_attention(w, anc, batches=batches, heads=list(range(heads)))
+    t_attn = time.perf_counter() - t0
+    cfg = SamplerCfg(temperature=spec.temperature, top_k=spec.top_k, top_p=spec.top_p,
+                     greedy=spec.greedy)
+    t1 = time.perf_counter()
+    sl = slice(0, len(batches))
+    if spec.is_tree:
+        oracle.sampler.accept_tree_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                         w.draft_tokens[sl].numpy(), w.parent[sl].numpy(),
+                                         w.uniforms[sl].numpy(), cfg)
+    else:
+        oracle.sampler.accept_chain_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                          w.draft_tokens[sl].numpy(), w.uniforms[sl].numpy(), cfg)
+    t_samp = time.perf_counter() - t1
+    scale_b = spec.B / len(batches)
+    return (t_attn * spec.Hq / heads + t_samp) * scale_b
+
+
+def cpu_baseline(spec, budget_s=15.0, device=None):
+    w = cpu_inputs(spec, device)
+    heads, batches = oracle_sample_plan(spec)
+    est, n, t0 = [], 0, time.perf_counter()
+    while n == 0 or (time.perf_counter() - t0 < budget_s and n < 20):
+        est.append(oracle_step(spec, w, heads, batches))
+        n += 1
+    step_s = statistics.fmean(est)
+    return {"value": spec.B * spec.R / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"{n} oracle step(s) of {spec.name}: sampler rows of {len(batches)} "
+                       f"sequence(s) and attention for {heads} of {spec.Hq} query heads, "
+                       f"scaled to the full step (B={spec.B}); numpy float64, one thread")}
+
+
+def bench_reference(args, spec):
+    w = cpu_inputs(spec)
+    heads, batches = oracle_sample_plan(spec)
+    for _ in range(args.warmup):
+        oracle_step(spec, w, heads, batches)
+    est = [oracle_step(spec, w, heads, batches) for _ in range(args.steps)]
+    step_s = statistics.fmean(est)
+    value = spec.B * spec.R / step_s
+    cb = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+          "sample": (f"each step: sampler rows of {len(batches)} sequence(s) and attention for "
+                     f"{heads} of {spec.Hq} query heads of {spec.name}, scaled to the full step")}
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": spec.name, "global_batch": spec.B},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.SPECS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    spec = wl.SPECS[args.workload]
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args, spec)), flush=True)
+        return 0
+
+    init_dist(ws, "nccl")
+    out = bench_gpu(args, spec, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(spec, device=torch.device("cuda", local))
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

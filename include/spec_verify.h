@@ -1,0 +1,245 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so, the target-side verification
+ * step of speculative decoding on one GPU (sm_103a).
+ *
+ * The step has two parts, both defined by the pages this library follows:
+ *
+ *   spec_verify_attn    one multi-row attention pass over the proposed block
+ *                       ("Drafters and Speculative Decoding: Useful Tokens,
+ *                       Correct State", section "From a proposed block to a
+ *                       causal target pass"), with a draft-tree visibility
+ *                       mask ("Speculative Decoding" (atlas), section
+ *                       "Chains, trees and visibility"), computed as split-K
+ *                       flash-decoding partials plus a log-sum-exp combine
+ *                       ("Speculative Token Decoupling: Asynchronous
+ *                       Verification via Flash-Decoding", section 03).
+ *   spec_accept_sample  the lossless acceptance sampler: target distribution
+ *                       p with temperature / top-k / top-p, left-to-right
+ *                       test u*q(x) < p(x) on shifted rows, residual
+ *                       norm(max(0, p - q)) at the first rejection, bonus
+ *                       token when every draft survives, greedy mode
+ *                       ("Speculative Decoding" (atlas), sections "One round
+ *                       and shifted logits", "Exact sampling: account for
+ *                       every probability", "Greedy, sampling and the real
+ *                       sampler"; "Drafters and Speculative Decoding",
+ *                       section "Sampling needs a correction rule").
+ *
+ * Conventions for every call:
+ *   - Array arguments are DEVICE pointers owned by the caller, in the layout
+ *     given beside each argument (row-major, innermost last).  The library
+ *     keeps no pointer after a call returns.
+ *   - The library allocates no memory.  Scratch comes from a caller-provided
+ *     workspace whose size a *_workspace_size() call returns.  Workspaces
+ *     hold self-resetting counters: zero-fill a workspace once when you
+ *     allocate it; every completed call leaves it ready for the next one.
+ *     Concurrent calls must not share a workspace.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No call synchronises.  Calls may be captured in CUDA graphs.
+ *   - Argument and shape errors are detected on the host before any launch
+ *     and return SPEC_EINVAL; shapes outside the supported envelope return
+ *     SPEC_EUNSUPPORTED; a failed launch returns SPEC_ECUDA.  Data-dependent
+ *     conditions are reported per sequence in status_per_seq (bits below).
+ *   - Device-side waits are bounded; a wait that runs out sets the error
+ *     word that spec_workspace_error() reads, and the call's outputs are then
+ *     unspecified.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_EINVAL = 1,        /* bad pointer, size or parameter */
+  SPEC_EUNSUPPORTED = 2,  /* valid request outside what the kernels implement */
+  SPEC_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+  SPEC_ETIMEOUT = 4       /* a bounded device-side wait ran out (error word) */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* status_per_seq bits (OR-ed). */
+#define SPEC_SEQ_QZERO 1       /* a proposed token had q(x) == 0; it was accepted iff p(x) > 0 */
+#define SPEC_SEQ_NONFINITE 2   /* a target logit was NaN or +inf; that sequence's outputs are -1 */
+#define SPEC_SEQ_RESID_ZERO 4  /* residual mass was 0 after a rejection; the draw used p */
+#define SPEC_SEQ_BAD_TREE 8    /* parent array is not a tree in storage order */
+
+/* Error words written to a workspace by a bounded wait that ran out. */
+#define SPEC_ERR_MBAR_TIMEOUT 0x100
+
+/* Human-readable name of a status code (static string). */
+const char* spec_status_str(spec_status s);
+
+/* ------------------------------------------------------------------------
+ * spec_tree_prepare -- visibility of a flattened draft tree.
+ * "Speculative Decoding" (atlas), "Chains, trees and visibility": each node
+ * sees the accepted prefix, its ancestors and itself; position ids follow
+ * depth; a parent array plus an ancestor mask state this.
+ *
+ *   parent   [B,R] int32, node 0 is the root/pending anchor (parent -1), every
+ *            other node i has 0 <= parent[i] < i.  NULL means a chain
+ *            (parent[i] = i - 1), the causal case.
+ *   ctx_len  [B] int32, committed tokens before the block (>= 0).
+ *   anc_mask [B,R] uint64 out: bit j set iff node j is node i or an ancestor.
+ *   pos_ids  [B,R] int32 out (nullable): ctx_len[b] + depth(i).
+ *   status_per_seq [B] int32 out (nullable): SPEC_SEQ_BAD_TREE if the parent
+ *            row breaks the rule above (mask/pos of that row are then 0).
+ *   1 <= R <= 64.
+ * ---------------------------------------------------------------------- */
+spec_status spec_tree_prepare(const int32_t* parent, const int32_t* ctx_len, int B, int R,
+                              uint64_t* anc_mask, int32_t* pos_ids, int32_t* status_per_seq,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_attn -- multi-row, tree-masked, paged GQA attention as split-K
+ * flash-decoding partials plus a log-sum-exp combine.
+ *
+ *   q          [B,R,Hq,D]   dtype (bf16, or fp32 for the CUDA-core path)
+ *   k_cache,
+ *   v_cache    [num_pages,page_size,Hkv,D] dtype; the R block rows of
+ *              sequence b are already stored at positions ctx_len[b] ..
+ *              ctx_len[b]+R-1 of its page list.
+ *   block_table[B,max_pages] int32: page ids of sequence b in order.  Entries
+ *              past the sequence's last page are not read.
+ *   ctx_len    [B] int32: committed positions, all visible to every row.
+ *   anc_mask   [B,R] uint64: block position ctx+j is visible to row i iff bit
+ *              j of anc_mask[b,i] is set (spec_tree_prepare's output).
+ *   scale      softmax scale; <= 0 selects 1/sqrt(D).
+ *   num_splits KV chunks per (sequence, KV head); 0 lets the library choose.
+ *   workspace  >= spec_verify_attn_workspace_size(...) bytes, 256-B aligned.
+ *   out        [B,R,Hq,D] dtype.
+ *   lse_out    [B,R,Hq] fp32 natural-log LSE of the scaled scores (nullable).
+ *
+ * Query head h reads KV head h / (Hq/Hkv).  Supported: D in {64,128};
+ * bf16 needs D == 128, page_size % 16 == 0, 16-byte aligned cache rows;
+ * fp32 any page_size; R*Hq/Hkv <= 512; R <= 64.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_attn_workspace_size(int B, int R, int Hq, int Hkv, int D, int page_size,
+                                       int max_pages, int num_splits);
+
+/* The split count the library would use (resolves num_splits == 0). */
+int spec_verify_attn_num_splits(int B, int R, int Hq, int Hkv, int D, int page_size,
+                                int max_pages, int num_splits);
+
+spec_status spec_verify_attn(const void* q, const void* k_cache, const void* v_cache,
+                             spec_dtype dtype, int page_size, int num_pages,
+                             const int32_t* block_table, int max_pages,
+                             const int32_t* ctx_len, const uint64_t* anc_mask,
+                             int B, int R, int Hq, int Hkv, int D, float scale, int num_splits,
+                             void* workspace, size_t workspace_bytes,
+                             void* out, float* lse_out, void* stream);
+
+/* The two phases of spec_verify_attn as separate calls, with the same
+ * arguments: spec_verify_attn_partials launches the split-K pass (one partial
+ * output and log-sum-exp per KV chunk, kept in `workspace`); a following
+ * spec_verify_attn_combine on the same stream, with the same shapes and
+ * workspace, merges them into `out` / `lse_out` ("Speculative Token
+ * Decoupling: Asynchronous Verification via Flash-Decoding", section 03:
+ * split-K attention).  The combine reads only ctx_len and the workspace;
+ * q, k_cache, v_cache, block_table and anc_mask may be NULL there. */
+spec_status spec_verify_attn_partials(const void* q, const void* k_cache, const void* v_cache,
+                                      spec_dtype dtype, int page_size, int num_pages,
+                                      const int32_t* block_table, int max_pages,
+                                      const int32_t* ctx_len, const uint64_t* anc_mask,
+                                      int B, int R, int Hq, int Hkv, int D, float scale,
+                                      int num_splits, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+spec_status spec_verify_attn_combine(const void* q, const void* k_cache, const void* v_cache,
+                                     spec_dtype dtype, int page_size, int num_pages,
+                                     const int32_t* block_table, int max_pages,
+                                     const int32_t* ctx_len, const uint64_t* anc_mask,
+                                     int B, int R, int Hq, int Hkv, int D, float scale,
+                                     int num_splits, void* workspace, size_t workspace_bytes,
+                                     void* out, float* lse_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sampler settings, as actually served ("Greedy, sampling and the real
+ * sampler": p and q must include the served transforms).
+ *   temperature > 0 (ignored when greedy);  top_k: 0 or >= V disables, else
+ *   the k largest logits stay (ties: lower id first);  top_p in (0,1]: 1
+ *   disables, else the shortest (prob desc, id asc) prefix of the top-k
+ *   distribution with mass >= top_p stays, crossing token included;
+ *   greedy != 0: argmax verification;  eos_id >= 0: emission stops after the
+ *   first EOS token (-1 disables).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  float temperature;
+  int32_t top_k;
+  float top_p;
+  int32_t greedy;
+  int32_t eos_id;
+} spec_sampler;
+
+size_t spec_accept_sample_workspace_size(int B, int R, int V);
+
+/* ------------------------------------------------------------------------
+ * spec_accept_sample -- chain verification of B sequences.
+ *
+ *   target_logits [B,R,V] fp32, R = gamma + 1: row 0 is scored after the
+ *                 pending anchor, row i after draft i; row i checks draft
+ *                 i+1 and row gamma gives the bonus (shifted logits).
+ *   draft_probs   [B,R-1,V] fp32: row i is the distribution that actually
+ *                 proposed draft i+1 (already transformed).  May be NULL in
+ *                 greedy mode.
+ *   draft_tokens  [B,R-1] int32 in [0,V).
+ *   uniforms      [B,R] fp32 in [0,1): u[i] tests draft i+1, u[R-1] is the
+ *                 single draw used by the correction or the bonus token.
+ *   accepted_len  [B] int32 out: drafts accepted (0..R-1).
+ *   emitted       [B,R] int32 out: accepted drafts then the correction or
+ *                 bonus token; -1 after the last emitted token.
+ *   p_out         [B,R,V] fp32 out (nullable): the target distribution p of
+ *                 every row (not written in greedy mode).
+ *   status_per_seq[B] int32 out (nullable): SPEC_SEQ_* bits.
+ *
+ * A token is accepted iff u*q(x) < p(x) (the event u < min(1, p/q)); the
+ * correction is the first id t whose ascending running sum of
+ * max(0, p - q) exceeds u_final * sum; the bonus draws from p the same way.
+ * 1 <= R <= 64, 1 <= V <= 409600.
+ * ---------------------------------------------------------------------- */
+spec_status spec_accept_sample(const float* target_logits, const float* draft_probs,
+                               const int32_t* draft_tokens, const float* uniforms,
+                               int B, int R, int V, const spec_sampler* cfg,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* accepted_len, int32_t* emitted, float* p_out,
+                               int32_t* status_per_seq, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_accept_sample_tree -- draft-tree verification.  The pages leave the
+ * tree rule open ("Chains, trees and visibility": a tree needs its own
+ * proposal and sampling rule); this library uses the multi-candidate form
+ * of the chain rule for children drawn i.i.d. from q at their parent: at
+ * node v (start: node 0, p' = p_0) try v's children in storage order; child
+ * c with token t is accepted iff u[c-1]*q_v(t) < p'(t), and the walk moves
+ * to c with p' = p_c; a rejected child sets p' = norm(max(0, p' - q_v)).
+ * With no accepted child the final token is drawn from p' with u[N-1].
+ *
+ *   target_logits [B,N,V] fp32: row v scored after node v.
+ *   draft_probs   [B,N,V] fp32: row v is the q that proposed v's children.
+ *   node_tokens   [B,N] int32 (node 0 unused);  parent [B,N] int32 as in
+ *                 spec_tree_prepare;  uniforms [B,N] fp32.
+ *   accepted_len  [B] out: accepted nodes on the path.
+ *   path_nodes    [B,N] out: accepted node ids, then -1.
+ *   emitted       [B,N] out: accepted tokens then the final token, then -1.
+ *   p_out, status_per_seq as above.  2 <= N <= 64.
+ * ---------------------------------------------------------------------- */
+spec_status spec_accept_sample_tree(const float* target_logits, const float* draft_probs,
+                                    const int32_t* node_tokens, const int32_t* parent,
+                                    const float* uniforms, int B, int N, int V,
+                                    const spec_sampler* cfg, void* workspace,
+                                    size_t workspace_bytes, int32_t* accepted_len,
+                                    int32_t* path_nodes, int32_t* emitted, float* p_out,
+                                    int32_t* status_per_seq, void* stream);
+
+/* Copy the workspace error word to *host_err (synchronises `stream`). */
+spec_status spec_workspace_error(const void* workspace, int32_t* host_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -44,13 +44,15 @@ def visible_positions(ctx: int, mask_word) -> np.ndarray:
 
 
 def verify_attention(q, k_cache, v_cache, block_table, ctx_len, anc_mask, scale=None,
-                     batches=None):
+                     batches=None, rows=None, heads=None):
     """Full-softmax attention of every (sequence, block row, query head).
 
     q [B,R,Hq,D]; k_cache, v_cache [pages, P, Hkv, D]; block_table [B, maxp];
     ctx_len [B]; anc_mask [B,R] (uint64 words).  Inputs are the values the GPU
     reads (bf16 inputs already widened); arithmetic is float64.
-    Returns out [B,R,Hq,D] and lse [B,R,Hq].
+    Returns out [B,R,Hq,D] and lse [B,R,Hq].  batches / rows / heads restrict
+    which outputs are computed (the others stay zero); the arithmetic of each
+    computed output is unchanged.
     """
     q = np.asarray(q, dtype=np.float64)
     k_cache = np.asarray(k_cache, dtype=np.float64)
@@ -66,9 +68,9 @@ def verify_attention(q, k_cache, v_cache, block_table, ctx_len, anc_mask, scale=
         ctx = int(ctx_len[b])
         K = gather_kv(k_cache, block_table[b], ctx + R)
         Vv = gather_kv(v_cache, block_table[b], ctx + R)
-        for i in range(R):
+        for i in (range(R) if rows is None else rows):
             vis = visible_positions(ctx, anc_mask[b][i])
-            for h in range(Hq):
+            for h in (range(Hq) if heads is None else heads):
                 kvh = h // G
                 s = K[vis, kvh, :] @ q[b, i, h] * scale
                 smax = s.max()

@@ -43,11 +43,14 @@ Readings where the pages are silent (each also listed in the design notes):
   * With eos_id >= 0, emission stops after the first EOS token, whether it is
     an accepted draft or the correction/bonus token.
 
-Decision flags: a sequence whose outcome sits within FLAG_EPS of a decision
-boundary is reported as flagged; bit-exact comparison skips flagged sequences.
+Decision flags: a sequence whose outcome depends on a decision taken within
+FLAG_EPS of its threshold is reported as flagged; bit-exact comparison skips
+flagged sequences.
   * ratio test: |u - p(x)/q(x)| < FLAG_EPS;
   * inverse-CDF draw: u * Z within FLAG_EPS * Z of the chosen token's edges;
-  * top-p: the cumulative mass at the cutoff (either side) within FLAG_EPS of top_p.
+  * top-p: every cutoff that running masses perturbed by up to FLAG_EPS could
+    select is tried; the sequence is flagged if any of them changes the
+    outcome (accepted length or emitted tokens) of the walk.
 """
 from dataclasses import dataclass
 
@@ -74,19 +77,45 @@ def _f32(x) -> float:
     return float(np.float32(x))
 
 
-def target_distribution(logits_row, cfg: SamplerCfg):
-    """p over the vocabulary for one target row.  Returns (p, flagged)."""
+MAX_ALTERNATIVES = 64
+
+
+def _p_from_kept(z, kept):
+    p = np.zeros(z.shape[0])
+    zk = z[kept]
+    e = np.exp(zk - zk.max())
+    p[kept] = e / e.sum()
+    return p
+
+
+def _ordered_kept(logits_row, cfg: SamplerCfg):
+    """z = logits / T and the top-k kept ids in (z desc, id asc) order."""
     l = np.asarray(logits_row, dtype=np.float64)
     V = l.shape[0]
     if np.any(np.isnan(l)) or np.any(l == np.inf):
         raise ValueError("non-finite target logit")
-    T = _f32(cfg.temperature)
-    top_p = _f32(cfg.top_p)
-    z = l / T
+    z = l / _f32(cfg.temperature)
     order = np.lexsort((np.arange(V), -z))          # z descending, then id ascending
     kept = order
     if 0 < cfg.top_k < V:
         kept = kept[:cfg.top_k]
+    return z, kept
+
+
+def p_for_cutoff(logits_row, cfg: SamplerCfg, m: int):
+    """p when top-p keeps exactly the first m tokens of the top-k order."""
+    z, kept = _ordered_kept(logits_row, cfg)
+    return _p_from_kept(z, kept[:m])
+
+
+def target_distribution(logits_row, cfg: SamplerCfg, alternatives=None):
+    """p over the vocabulary for one target row.  Returns (p, flagged).
+
+    If `alternatives` is a list, the sizes of the other top-p cutoffs within
+    FLAG_EPS (see the module docstring) are appended to it; more than
+    MAX_ALTERNATIVES of them set the flag instead."""
+    z, kept = _ordered_kept(logits_row, cfg)
+    top_p = _f32(cfg.top_p)
     flagged = False
     if 0.0 < top_p < 1.0:
         zk = z[kept]
@@ -94,13 +123,18 @@ def target_distribution(logits_row, cfg: SamplerCfg):
         c = np.cumsum(e / e.sum())
         reach = np.nonzero(c >= top_p)[0]
         n = int(reach[0]) + 1 if reach.size else len(kept)
-        flagged = abs(c[n - 1] - top_p) < FLAG_EPS or (n >= 2 and abs(c[n - 2] - top_p) < FLAG_EPS)
+        # prefix lengths m that are "first to reach top_p" for some running
+        # masses within FLAG_EPS of the exact ones
+        prev = np.concatenate([[-np.inf], c[:-1]])
+        cand = np.nonzero((c >= top_p - FLAG_EPS) & (prev < top_p + FLAG_EPS))[0] + 1
+        others = [int(m) for m in cand if m != n]
+        if others:
+            if alternatives is None or len(others) > MAX_ALTERNATIVES:
+                flagged = True
+            else:
+                alternatives.extend(others)
         kept = kept[:n]
-    p = np.zeros(V)
-    zk = z[kept]
-    e = np.exp(zk - zk.max())
-    p[kept] = e / e.sum()
-    return p, flagged
+    return _p_from_kept(z, kept), flagged
 
 
 def inverse_cdf(w, u):
@@ -195,14 +229,30 @@ def accept_chain(logits, q_rows, drafts, u, cfg: SamplerCfg):
         res = greedy_walk(logits, drafts, cfg.eos_id)
         res["p"] = None
         return res
-    p_rows, pflag = [], False
+    p_rows, alts, pflag = [], [], False
     for i in range(len(logits)):
-        p, fl = target_distribution(logits[i], cfg)
+        a = []
+        p, fl = target_distribution(logits[i], cfg, a)
         p_rows.append(p)
+        alts.append(a)
         pflag |= fl
     res = chain_walk(p_rows, q_rows, drafts, u, cfg.eos_id)
-    res["flagged"] = res["flagged"] or pflag
+    flagged = res["flagged"] or pflag
+    # rows the walk read: 0 .. last row it used; a near-threshold top-p cutoff
+    # there flags the sequence only if moving the cutoff changes the outcome
+    last_row = min(res["accepted_len"], len(p_rows) - 1)
+    for i in range(last_row + 1):
+        for m in alts[i]:
+            if flagged:
+                break
+            trial = list(p_rows)
+            trial[i] = p_for_cutoff(logits[i], cfg, m)
+            r2 = chain_walk(trial, q_rows, drafts, u, cfg.eos_id)
+            if r2["accepted_len"] != res["accepted_len"] or r2["emitted"] != res["emitted"]:
+                flagged = True
+    res["flagged"] = flagged
     res["p"] = np.stack(p_rows)
+    res["alt_sizes"] = alts
     return res
 
 
@@ -276,14 +326,27 @@ def accept_tree(logits, q_nodes, tokens, parent, u, cfg: SamplerCfg):
             v = nxt[0]
         return dict(accepted_len=len(path), path=path, emitted=emitted, flagged=False,
                     status=0, p=None)
-    p_nodes, pflag = [], False
+    p_nodes, alts, pflag = [], [], False
     for i in range(N):
-        p, fl = target_distribution(logits[i], cfg)
+        a = []
+        p, fl = target_distribution(logits[i], cfg, a)
         p_nodes.append(p)
+        alts.append(a)
         pflag |= fl
     res = tree_walk(p_nodes, q_nodes, tokens, parent, u, cfg.eos_id)
-    res["flagged"] = res["flagged"] or pflag
+    flagged = res["flagged"] or pflag
+    for v in [0] + list(res["path"]):              # nodes whose p the walk read
+        for m in alts[v]:
+            if flagged:
+                break
+            trial = list(p_nodes)
+            trial[v] = p_for_cutoff(logits[v], cfg, m)
+            r2 = tree_walk(trial, q_nodes, tokens, parent, u, cfg.eos_id)
+            if r2["path"] != res["path"] or r2["emitted"] != res["emitted"]:
+                flagged = True
+    res["flagged"] = flagged
     res["p"] = np.stack(p_nodes)
+    res["alt_sizes"] = alts
     return res
 
 
@@ -305,6 +368,7 @@ def accept_chain_batch(logits, q, drafts, u, cfg: SamplerCfg, want_p=False):
                status=np.array([r["status"] for r in res]))
     if want_p and res and res[0]["p"] is not None:
         out["p"] = np.stack([r["p"] for r in res])
+        out["alt_sizes"] = [r["alt_sizes"] for r in res]
     return out
 
 
@@ -320,4 +384,5 @@ def accept_tree_batch(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=Fals
                status=np.array([r["status"] for r in res]))
     if want_p and res and res[0]["p"] is not None:
         out["p"] = np.stack([r["p"] for r in res])
+        out["alt_sizes"] = [r["alt_sizes"] for r in res]
     return out

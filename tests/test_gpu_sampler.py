@@ -1,0 +1,317 @@
+"""GPU parity: the acceptance sampler against the oracle.
+
+accepted_len and emitted tokens must match bit-exactly on every sequence the
+oracle does not flag (a decision within 1e-5 of its threshold); flagged
+sequences are counted and must still produce a valid outcome.  p must match
+within 1e-6 relative.  Statistical tests check the lossless property and the
+closed form of the expected tokens per step on the GPU kernel itself.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+import speculative_decoding_verification_76_gb300 as sv
+from oracle.sampler import SamplerCfg
+from speculative_decoding_verification_76_gb300 import workloads as wl
+from tests.conftest import load_golden
+from tests.util import P_RTOL, cfg_of
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _api_cfg(c: SamplerCfg) -> sv.SamplerConfig:
+    return sv.SamplerConfig(temperature=c.temperature, top_k=c.top_k, top_p=c.top_p,
+                            greedy=c.greedy, eos_id=c.eos_id)
+
+
+def run_chain(logits, q, drafts, u, cfg: SamplerCfg, want_p=True):
+    t = lambda a: None if a is None else torch.as_tensor(a).to(DEV).contiguous()  # noqa: E731
+    res = sv.accept_sample(t(logits), t(q), t(drafts), t(u), _api_cfg(cfg),
+                           want_p=want_p and not cfg.greedy)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def run_tree(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=True):
+    t = lambda a: None if a is None else torch.as_tensor(a).to(DEV).contiguous()  # noqa: E731
+    res = sv.accept_sample_tree(t(logits), t(q), t(tokens), t(parent), t(u), _api_cfg(cfg),
+                                want_p=want_p and not cfg.greedy)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def compare(gpu, ref, tree=False, max_flag_frac=0.5):
+    ok = ~ref["flagged"]
+    assert ok.mean() >= 1 - max_flag_frac, f"too many flagged: {ref['flagged'].sum()}"
+    np.testing.assert_array_equal(gpu["accepted_len"][ok], ref["accepted_len"][ok])
+    np.testing.assert_array_equal(gpu["emitted"][ok], ref["emitted"][ok])
+    if tree:
+        np.testing.assert_array_equal(gpu["path"][ok], ref["path"][ok])
+    # flagged sequences: still a valid outcome (accepted prefix of the drafts)
+    assert (gpu["accepted_len"] >= 0).all()
+    return int(ref["flagged"].sum())
+
+
+def check_p(gpu_p, ref, logits=None, cfg=None):
+    """p within P_RTOL relative.  Where the oracle found the top-p cutoff
+    ambiguous (within 1e-5), the GPU may keep one of the other sizes; it is
+    then compared with the oracle's p for that size."""
+    ref_p = np.asarray(ref["p"])
+    B, R, _ = ref_p.shape
+    for b in range(B):
+        for i in range(R):
+            rp = ref_p[b, i]
+            gp = gpu_p[b, i].astype(np.float64)
+            n_gpu = int((gp > 0).sum())
+            if n_gpu != int((rp > 0).sum()) and logits is not None:
+                alts = ref.get("alt_sizes", [[[]] * R] * B)[b][i]
+                assert n_gpu in alts, f"row {b},{i}: kept {n_gpu} not an ambiguous cutoff {alts}"
+                rp = oracle.sampler.p_for_cutoff(np.asarray(logits)[b, i], cfg, n_gpu)
+            err = np.abs(gp - rp)
+            bad = err > P_RTOL * rp + 1e-38
+            assert not bad.any(), (b, i, np.argwhere(bad)[:5],
+                                   (err / np.maximum(rp, 1e-300)).max())
+            assert ((gp == 0) == (rp == 0)).all(), f"kept sets differ in row {b},{i}"
+
+
+def chain_case(spec, seed, greedy=False, eos=-1, want_p=True):
+    w = wl.make_sampler_inputs(spec, seed=seed)
+    cfg = cfg_of(spec, greedy=greedy, eos=eos)
+    gpu = run_chain(w.logits, None if greedy else w.draft_probs, w.draft_tokens, w.uniforms, cfg,
+                    want_p)
+    ref = oracle.sampler.accept_chain_batch(w.logits.numpy(), w.draft_probs.numpy(),
+                                            w.draft_tokens.numpy(), w.uniforms.numpy(), cfg,
+                                            want_p=want_p and not greedy)
+    return w, gpu, ref
+
+
+# ------------------------------------------------------------------ worked examples on the GPU
+def test_three_token_example_on_gpu():
+    g = load_golden("three_token.json")["solved_from_printed"]
+    p, q = np.array(g["p"]), np.array(g["q"])
+    B = 8192
+    rng = np.random.default_rng(1)
+    logits = np.tile(np.log(p).astype(np.float32), (B, 2, 1))
+    qq = np.tile(q.astype(np.float32), (B, 1, 1))
+    drafts = rng.choice(3, size=(B, 1), p=q).astype(np.int32)
+    u = (rng.integers(0, 1 << 24, size=(B, 2)) / (1 << 24)).astype(np.float32)
+    gpu = run_chain(logits, qq, drafts, u, SamplerCfg(), want_p=True)
+    ref = oracle.sampler.accept_chain_batch(logits, qq, drafts, u, SamplerCfg(), want_p=True)
+    compare(gpu, ref)
+    check_p(gpu["p"], ref, logits, SamplerCfg())
+    first = np.bincount(gpu["emitted"][:, 0], minlength=3)
+    assert stats.chisquare(first, p * B).pvalue > 1e-3
+
+
+def test_chain_bird_on_gpu():
+    g = load_golden("chain_bird.json")
+    c = g["constructed_distributions"]
+    with np.errstate(divide="ignore"):
+        logits = np.log(np.array(c["p_rows"], dtype=np.float64)).astype(np.float32)[None]
+    q = np.array(c["q_rows"], dtype=np.float32)[None]
+    drafts = np.array([c["drafts"]], dtype=np.int32)
+    for u in ([0.0] * 5, [0.999] * 5, [0.3, 0.7, 0.1, 0.9, 0.42]):
+        gpu = run_chain(logits, q, drafts, np.array([u], dtype=np.float32), SamplerCfg())
+        assert gpu["accepted_len"][0] == g["expected"]["accepted_len"]
+        assert gpu["emitted"][0, :3].tolist() == g["expected"]["emitted"]
+        assert gpu["emitted"][0, 3:].tolist() == [-1, -1]
+
+
+# ------------------------------------------------------------------ configurations
+def test_tiny_chain_exact_config():
+    spec = wl.SPECS["tiny_chain"]
+    for seed in range(20):
+        w, gpu, ref = chain_case(spec, seed)
+        compare(gpu, ref)
+        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+
+
+SMALL = [
+    ("temp", dict(temperature=0.8)),
+    ("topk", dict(temperature=0.7, top_k=50)),
+    ("topp", dict(temperature=1.0, top_p=0.9)),
+    ("topk_topp", dict(temperature=0.9, top_k=200, top_p=0.8)),
+    ("sharp", dict(temperature=0.25, top_p=0.5)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("V", [1000, 4099, 40000])
+def test_small_batches(name, kw, V):
+    spec = wl.Spec(name, B=48, Hq=1, Hkv=1, D=64, V=V, ctx=(1, 1), gamma=7, logit_sd=3.0,
+                   draft_div=kw.get("temperature", 1.0), draft_noise=0.8, **kw)
+    nflag = 0
+    for seed in range(2):
+        w, gpu, ref = chain_case(spec, 10 * seed + V % 7)
+        nflag += compare(gpu, ref)
+        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+
+
+def test_greedy_small_and_ties():
+    spec = wl.Spec("g", B=64, Hq=1, Hkv=1, D=64, V=3001, ctx=(1, 1), gamma=6, temperature=0.8,
+                   greedy=True)
+    w = wl.make_sampler_inputs(spec, seed=4)
+    # integer logits: many exact ties; lowest id must win
+    logits = torch.round(w.logits).contiguous()
+    am = logits.argmax(-1)
+    drafts = am[:, :-1].clone().to(torch.int32)
+    drafts[::3, 2] = (drafts[::3, 2] + 1) % spec.V     # some mismatches
+    cfg = SamplerCfg(greedy=True)
+    gpu = run_chain(logits.numpy(), None, drafts.numpy(), w.uniforms.numpy(), cfg)
+    ref = oracle.sampler.accept_chain_batch(logits.numpy(), None, drafts.numpy(),
+                                            w.uniforms.numpy(), cfg)
+    compare(gpu, ref)
+
+
+def test_topk_with_ties_and_banned_tokens():
+    rng = np.random.default_rng(9)
+    B, R, V = 32, 4, 777
+    logits = rng.integers(-4, 5, size=(B, R, V)).astype(np.float32)   # heavy ties
+    logits[:, :, ::11] = -np.inf                                        # banned tokens
+    q = rng.dirichlet(np.ones(V), size=(B, R - 1)).astype(np.float32)
+    q[:, :, ::11] = 0
+    q /= q.sum(-1, keepdims=True)
+    q64 = q.astype(np.float64)
+    q64 /= q64.sum(-1, keepdims=True)
+    drafts = np.stack([[rng.choice(V, p=q64[b, i]) for i in range(R - 1)]
+                       for b in range(B)]).astype(np.int32)
+    u = (rng.integers(0, 1 << 24, size=(B, R)) / (1 << 24)).astype(np.float32)
+    for cfg in (SamplerCfg(top_k=7), SamplerCfg(top_k=100, top_p=0.6), SamplerCfg(top_p=0.3)):
+        gpu = run_chain(logits, q, drafts, u, cfg)
+        ref = oracle.sampler.accept_chain_batch(logits, q, drafts, u, cfg, want_p=True)
+        compare(gpu, ref)
+        check_p(gpu["p"], ref, logits, cfg)
+
+
+def test_eos_and_q_zero_and_short_blocks():
+    rng = np.random.default_rng(3)
+    V = 50
+    # R = 1: no drafts, only the bonus draw
+    logits = rng.normal(0, 2, size=(16, 1, V)).astype(np.float32)
+    u = rng.random((16, 1)).astype(np.float32)
+    gpu = run_chain(logits, np.zeros((16, 0, V), np.float32), np.zeros((16, 0), np.int32), u,
+                    SamplerCfg())
+    ref = oracle.sampler.accept_chain_batch(logits, np.zeros((16, 0, V)), np.zeros((16, 0), int),
+                                            u, SamplerCfg())
+    compare(gpu, ref)
+    # EOS accepted inside the block: emission stops there
+    p = np.full(V, 1.0 / V, dtype=np.float32)
+    logits = np.zeros((2, 4, V), np.float32)
+    q = np.tile(p, (2, 3, 1))
+    drafts = np.array([[5, 7, 3], [1, 2, 7]], np.int32)
+    u = np.full((2, 4), 0.2, np.float32)
+    gpu = run_chain(logits, q, drafts, u, SamplerCfg(eos_id=7))
+    assert gpu["accepted_len"].tolist() == [2, 3]
+    assert gpu["emitted"].tolist() == [[5, 7, -1, -1], [1, 2, 7, -1]]
+    # q(x) = 0 < p(x): accepted, reported
+    q0 = np.tile(p, (1, 1, 1))
+    q0[0, 0, 9] = 0.0
+    gpu = run_chain(np.zeros((1, 2, V), np.float32), q0, np.array([[9]], np.int32),
+                    np.array([[0.5, 0.5]], np.float32), SamplerCfg())
+    assert gpu["accepted_len"][0] == 1 and gpu["status"][0] & sv.api.SEQ_QZERO
+
+
+def test_nonfinite_logits_are_reported():
+    logits = np.zeros((2, 3, 64), np.float32)
+    logits[1, 1, 5] = np.nan
+    q = np.full((2, 2, 64), 1 / 64, np.float32)
+    gpu = run_chain(logits, q, np.zeros((2, 2), np.int32), np.full((2, 3), 0.5, np.float32),
+                    SamplerCfg())
+    assert gpu["status"][1] & sv.api.SEQ_NONFINITE and gpu["accepted_len"][1] == -1
+    assert (gpu["emitted"][1] == -1).all()
+    assert gpu["status"][0] == 0 and gpu["accepted_len"][0] == 2
+
+
+@pytest.mark.parametrize("name", ["llama8b_chain", "long_context"])
+def test_full_vocab_chain(name):
+    spec = wl.SPECS[name].with_(B=6)
+    flagged = 0
+    for greedy in (False, True):
+        w, gpu, ref = chain_case(spec, 5, greedy=greedy, want_p=not greedy)
+        flagged += compare(gpu, ref)
+        if not greedy:
+            check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+
+
+def test_batched_serving_topp_sample():
+    for name in ("batched_serving_a45", "batched_serving_a75"):
+        spec = wl.SPECS[name].with_(B=8)
+        w, gpu, ref = chain_case(spec, 3)
+        compare(gpu, ref)
+        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+
+
+# ------------------------------------------------------------------ tree
+def tree_case(spec, seed, greedy=False, want_p=True):
+    w = wl.make_sampler_inputs(spec, seed=seed)
+    cfg = cfg_of(spec, greedy=greedy)
+    gpu = run_tree(w.logits, None if greedy else w.draft_probs, w.draft_tokens, w.parent,
+                   w.uniforms, cfg, want_p)
+    ref = oracle.sampler.accept_tree_batch(w.logits.numpy(), w.draft_probs.numpy(),
+                                           w.draft_tokens.numpy(), w.parent.numpy(),
+                                           w.uniforms.numpy(), cfg, want_p=want_p and not greedy)
+    return w, gpu, ref
+
+
+@pytest.mark.parametrize("top_k", [0, 50])
+def test_tree_small(top_k):
+    spec = wl.Spec("tree", B=24, Hq=1, Hkv=1, D=64, V=2000, ctx=(1, 1), tree_nodes=20,
+                   tree_depth=4, temperature=0.7, top_k=top_k, draft_div=0.7, draft_noise=0.5)
+    for seed in range(2):
+        w, gpu, ref = tree_case(spec, seed)
+        compare(gpu, ref, tree=True)
+        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+    w, gpu, ref = tree_case(spec, 7, greedy=True)
+    compare(gpu, ref, tree=True)
+
+
+def test_tree_draft_tree_config():
+    spec = wl.SPECS["draft_tree"]
+    w, gpu, ref = tree_case(spec, spec.seed)
+    compare(gpu, ref, tree=True)
+    check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+
+
+def test_tree_first_token_follows_p_root_on_gpu():
+    rng = np.random.default_rng(7)
+    V, B = 6, 12000
+    p_root = np.array([0.35, 0.25, 0.2, 0.1, 0.1, 0.0])
+    q_root = np.array([0.05, 0.4, 0.05, 0.3, 0.0, 0.2])
+    N = 5
+    parent = np.tile(np.array([-1, 0, 0, 0, 1], np.int32), (B, 1))
+    with np.errstate(divide="ignore"):
+        lp = np.log(p_root).astype(np.float32)
+    logits = np.tile(lp, (B, N, 1))
+    q = np.tile(q_root.astype(np.float32), (B, N, 1))
+    toks = np.concatenate([np.full((B, 1), -1), rng.choice(V, size=(B, 4), p=q_root)], 1)
+    toks = toks.astype(np.int32)
+    u = (rng.integers(0, 1 << 24, size=(B, N)) / (1 << 24)).astype(np.float32)
+    gpu = run_tree(logits, q, toks, parent, u, SamplerCfg(), want_p=False)
+    first = np.bincount(gpu["emitted"][:, 0], minlength=V)
+    assert first[5] == 0
+    assert stats.chisquare(first[:5], p_root[:5] * B).pvalue > 1e-3
+
+
+# ------------------------------------------------------------------ closed form on the GPU
+@pytest.mark.parametrize("gamma", [4, 7])
+def test_expected_tokens_closed_form_on_gpu(gamma):
+    g = load_golden("alpha08.json")["constructed_instance"]
+    p, q = np.array(g["p"]), np.array(g["q"])
+    alpha = np.minimum(p, q).sum()
+    B = 60000 // (gamma + 1)
+    rng = np.random.default_rng(gamma)
+    logits = np.tile(np.log(p).astype(np.float32), (B, gamma + 1, 1))
+    qq = np.tile(q.astype(np.float32), (B, gamma, 1))
+    drafts = rng.choice(3, size=(B, gamma), p=q).astype(np.int32)
+    u = (rng.integers(0, 1 << 24, size=(B, gamma + 1)) / (1 << 24)).astype(np.float32)
+    gpu = run_chain(logits, qq, drafts, u, SamplerCfg(), want_p=False)
+    n = (gpu["emitted"] >= 0).sum(1)
+    assert n.min() >= 1 and n.max() <= gamma + 1
+    expect = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(n.mean() - expect) < 4 * n.std() / math.sqrt(B), (n.mean(), expect)
+    assert np.array_equal(n - 1, gpu["accepted_len"])

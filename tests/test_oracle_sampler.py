@@ -239,9 +239,31 @@ def test_topp_minimal_prefix_includes_crossing_token():
     assert not fl
     p, fl = osm.target_distribution(logits, SamplerCfg(top_p=0.75))
     np.testing.assert_allclose(p, [4 / 9, 3 / 9, 2 / 9, 0], rtol=1e-6)
-    # a cutoff that lands on the boundary is flagged
+    # a cutoff that lands on the boundary is ambiguous: without room for
+    # alternatives it is flagged, with room the other cutoff is offered
     p, fl = osm.target_distribution(logits, SamplerCfg(top_p=0.7))
     assert fl
+    alts = []
+    p, fl = osm.target_distribution(logits, SamplerCfg(top_p=0.7), alts)
+    assert not fl and len(alts) == 1
+    assert {int((p > 0).sum()), alts[0]} == {2, 3}
+    alt = osm.p_for_cutoff(logits, SamplerCfg(top_p=0.7), alts[0])
+    assert int((alt > 0).sum()) == alts[0] and alt.sum() == pytest.approx(1.0)
+
+
+def test_topp_ambiguity_flags_only_when_outcome_changes():
+    # p over 4 tokens with a cutoff on the boundary between 2 and 3 kept
+    logits = np.log(np.array([0.4, 0.3, 0.2, 0.1])).astype(np.float32)
+    cfg = SamplerCfg(top_p=0.7)
+    q = np.array([0.25, 0.25, 0.25, 0.25])
+    # draft 0 accepted for any u (p/q > 1 either way), bonus drawn with u = 0.1
+    # from a row whose cutoff is unambiguous -> outcome is robust
+    rob = osm.accept_chain(np.stack([logits, np.log(np.array([.97, .01, .01, .01])).astype(np.float32)]),
+                           [q], [0], [0.5, 0.1], cfg)
+    assert not rob["flagged"]
+    # draft 2 is kept only under the 3-token cutoff: the outcome depends on it
+    amb = osm.accept_chain(np.stack([logits, logits]), [q], [2], [0.5, 0.1], cfg)
+    assert amb["flagged"]
 
 
 def test_topk_then_topp_and_temperature():
