@@ -159,6 +159,41 @@ spec_status spec_verify_attn_combine(const void* q, const void* k_cache, const v
                                      void* out, float* lse_out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_verify_attn_noalloc -- spec_verify_attn for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * Some callers cannot provide a workspace: a host application that passes a
+ * plugin nothing but its input and output buffers, a serving loop that may
+ * not allocate once it has started (its memory budget is fixed), or code
+ * that must not touch an allocator while the GPU is in use by others.  This
+ * call takes the same arguments as spec_verify_attn minus the workspace and
+ * keeps its split-K scratch in a fixed array of SPEC_NOALLOC_SCRATCH_BYTES
+ * compiled into the library.  That array occupies memory on every GPU that
+ * loads the library until the process exits.
+ *
+ *   - It allocates nothing and calls no allocating routine.  The first call on
+ *     each device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Problems whose scratch (spec_verify_attn_workspace_size) exceeds
+ *     SPEC_NOALLOC_SCRATCH_BYTES are refused with SPEC_EUNSUPPORTED before any
+ *     launch; use spec_verify_attn with your own workspace for those.
+ *   - All calls share the one array and it keeps whatever the last call left
+ *     there.  Calls whose GPU work overlaps (different streams, or different
+ *     host threads on one device without ordering) race on it and give wrong
+ *     results: order them on one stream.
+ *   - Results equal spec_verify_attn's for the same arguments.
+ * ---------------------------------------------------------------------- */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+spec_status spec_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     spec_dtype dtype, int page_size, int num_pages,
+                                     const int32_t* block_table, int max_pages,
+                                     const int32_t* ctx_len, const uint64_t* anc_mask,
+                                     int B, int R, int Hq, int Hkv, int D, float scale,
+                                     int num_splits, void* out, float* lse_out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Sampler settings, as actually served ("Greedy, sampling and the real
  * sampler": p and q must include the served transforms).
  *   temperature > 0 (ignored when greedy);  top_k: 0 or >= V disables, else

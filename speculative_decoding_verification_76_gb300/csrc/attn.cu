@@ -715,3 +715,64 @@ extern "C" spec_status spec_verify_attn_combine(SPEC_ATTN_ARGS, void* out, float
                                                 void* stream) {
   return verify_attn_impl(SPEC_ATTN_FWD, out, lse_out, stream, kCombine);
 }
+
+// ------------------------------------------------------------------ allocation-free variant
+// spec_verify_attn_noalloc runs exactly the work of spec_verify_attn, but its
+// split-K partials live in a fixed array compiled into this library instead
+// of a caller-provided workspace.  It exists for callers that cannot make a
+// device allocation at the point where they call us -- for example a host
+// that only hands a plugin its input and output buffers, or a serving loop
+// whose memory budget is frozen after start-up.  The array is reserved on
+// every GPU that loads the library and stays there until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The first call
+// on a device looks it up (cudaGetSymbolAddress, with that device current);
+// later calls reuse the cached address.  No memory is allocated.
+spec_status noalloc_scratch(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ECUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SPEC_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" spec_status spec_verify_attn_noalloc(const void* q, const void* k_cache,
+                                                const void* v_cache, spec_dtype dtype,
+                                                int page_size, int num_pages,
+                                                const int32_t* block_table, int max_pages,
+                                                const int32_t* ctx_len, const uint64_t* anc_mask,
+                                                int B, int R, int Hq, int Hkv, int D, float scale,
+                                                int num_splits, void* out, float* lse_out,
+                                                void* stream) {
+  if (B < 0) return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  const size_t need = spec_verify_attn_workspace_size(B, R, Hq, Hkv, D, page_size, max_pages,
+                                                      num_splits);
+  if (need == 0) return SPEC_EINVAL;
+  if (need > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_EUNSUPPORTED;  // too big for the array
+  void* scratch = nullptr;
+  const spec_status rs = noalloc_scratch(&scratch);
+  if (rs != SPEC_OK) return rs;
+  // the error word at the head of the scratch must start at zero on every call
+  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return SPEC_ECUDA;
+  return verify_attn_impl(q, k_cache, v_cache, dtype, page_size, num_pages, block_table,
+                          max_pages, ctx_len, anc_mask, B, R, Hq, Hkv, D, scale, num_splits,
+                          scratch, SPEC_NOALLOC_SCRATCH_BYTES, out, lse_out, stream, kBoth);
+}
