@@ -235,7 +235,7 @@ size_t spec_accept_sample_workspace_size(int B, int R, int V);
  * A token is accepted iff u*q(x) < p(x) (the event u < min(1, p/q)); the
  * correction is the first id t whose ascending running sum of
  * max(0, p - q) exceeds u_final * sum; the bonus draws from p the same way.
- * 1 <= R <= 64, 1 <= V <= 409600.
+ * 1 <= R <= 64, 1 <= V <= 172032.
  * ---------------------------------------------------------------------- */
 spec_status spec_accept_sample(const float* target_logits, const float* draft_probs,
                                const int32_t* draft_tokens, const float* uniforms,

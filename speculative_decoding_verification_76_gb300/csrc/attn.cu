@@ -28,11 +28,12 @@
 
 namespace {
 
-constexpr int kStageTokens = 64;
-constexpr int kStageBytes = 4 * 8192;  // K lo/hi + V lo/hi, 64 tokens x 128 B each
-constexpr int kNumStages = 4;
+constexpr int kStageTokens = 64;       // granularity of chunks (and the fp32 path)
+constexpr int kMaxStages = 6;
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kProducerWarps = 4;
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kQStride = 136;  // bf16 per Q row in shared memory (272 B: conflict-free ldmatrix)
 constexpr int kMaxChunk = 4096;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -42,6 +43,8 @@ struct AttnParams {
   const float* qf;         // fp32 path
   const float* kf;
   const float* vf;
+  const void* k;  // bf16 caches
+  const void* v;
   const int32_t* block_table;
   const int32_t* ctx_len;
   const uint64_t* anc_mask;
@@ -54,12 +57,30 @@ struct AttnParams {
 };
 
 // ------------------------------------------------------------------ bf16 tensor-core kernel
+// Stages in the K/V ring: as many as fit beside the Q tile (<= 227 KB).
+// Tokens per ring stage: 128 for 32-row tiles (more independent MMA tiles per
+// warp per stage), 64 when the accumulators of larger row tiles leave no room.
 template <int NRG>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_partial_bf16(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
-  constexpr int NTG = kConsumerWarps / NRG;
+__host__ __device__ constexpr int stage_tokens() {
+  return NRG == 2 ? 128 : 64;
+}
+// Stages in the ring: as many as fit beside the Q tile (<= 227 KB).
+template <int NRG>
+__host__ __device__ constexpr int stages_for() {
+  return NRG == 2 ? 3 : (NRG >= 8 ? 5 : 6);
+}
+
+template <int NRG>
+__global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParams p) {
+  static_assert(NRG >= 2, "a warp needs at least 16 tokens of every stage");
+  constexpr int NTG = kConsumerWarps / NRG;   // token sub-blocks of each stage
+  constexpr int ST = stage_tokens<NRG>();    // tokens per stage
+  constexpr int H = ST * 128;                // bytes of one K or V half-row block (64 dims)
+  constexpr int kStageBytes = 4 * H;         // K lo/hi + V lo/hi
+  constexpr int TS = ST / NTG;               // tokens of a stage handled by one warp
+  constexpr int NT = TS / 8;                  // 8-token MMA n-tiles per warp per stage
   constexpr int RT = 16 * NRG;
+  constexpr int kNumStages = stages_for<NRG>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -68,29 +89,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* bt_s = reinterpret_cast<int32_t*>(qs + RT * kQStride);          // chunk/16 + 1
   uint64_t* full = reinterpret_cast<uint64_t*>(bt_s + kMaxChunk / 16 + 8);
   uint64_t* empty = full + kNumStages;
+  static_assert(kNumStages * kStageBytes >= kConsumerWarps * 16 * (128 + 2) * 4,
+                "epilogue scratch must fit in the stage ring");
 
-  const int s = blockIdx.x;
-  const int kvh = blockIdx.y % p.Hkv;
-  const int rt = blockIdx.y / p.Hkv;
+  // KV heads are fastest in the grid: CTAs of all heads of the same tokens run
+  // together and use whole 2 KB token rows of the cache between them
+  const int kvh = blockIdx.x % p.Hkv;
+  const int rt = blockIdx.x / p.Hkv;
+  const int s = blockIdx.y;
   const int b = blockIdx.z;
   const int ctx = p.ctx_len[b];
   const int kv_len = ctx + p.R;
   const int c0 = s * p.chunk;
   if (c0 >= kv_len) return;  // this sequence needs fewer chunks
   const int c1 = min(c0 + p.chunk, kv_len);
-  const int nst = (c1 - c0 + kStageTokens - 1) / kStageTokens;
+  const int nst = (c1 - c0 + ST - 1) / ST;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // let a dependent grid (the LSE combine) start launching; it waits for
+  // this grid's completion before it reads any partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], NRG);
+      mbar_init(&full[i], kProducerThreads);   // one arrive per producer thread per stage
+      mbar_init(&empty[i], kConsumerWarps);
     }
     fence_mbar_init();
   }
-  // Q tile: row rho = i*G + g of this KV head -> q[b, i, kvh*G + g, :]
-  for (int idx = threadIdx.x; idx < RT * 16; idx += kThreads) {
+  __syncthreads();  // barriers initialised before anyone waits on them
+
+  if (warp >= kConsumerWarps) {
+    // ---------------- producer warps: the block-table slice, then K/V stages
+    // through 16-byte cp.async (L2 -> shared, L1 bypassed) into the swizzled
+    // stage layout; each thread's copies complete on the stage's mbarrier.
+    const int pt = threadIdx.x - 32 * kConsumerWarps;   // 0 .. 127
+    static_assert(kProducerThreads == 128, "16 columns x 8 token lanes");
+    const int P = p.page_size;
+    const int pg0 = c0 / P;
+    const int npg = (c1 - 1) / P - pg0 + 1;
+    // entries past the table width (a caller error) read as -1 and are
+    // zero-filled below instead of touching foreign memory
+    for (int i = pt; i < npg; i += kProducerThreads)
+      bt_s[i] = (pg0 + i < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + pg0 + i] : -1;
+    asm volatile("bar.sync 2, %0;" ::"n"(kProducerThreads) : "memory");
+    // Thread pt owns 16-byte column ch of token lanes tl, tl + 8, ..., tl + 56
+    // of every stage (K and V): its swizzled column offset is fixed, a page
+    // lookup is needed once per token, and each copy is two adds.
+    const int ch = pt & 15, tl = pt >> 4;
+    const uint32_t col = (uint32_t)((ch >> 3) * H + (((ch & 7) ^ tl) << 4));
+    const size_t tok_stride = (size_t)p.Hkv * 256;   // bytes between consecutive cache rows
+    const uint8_t* kcol = reinterpret_cast<const uint8_t*>(p.k) + (size_t)kvh * 256 + ch * 16;
+    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(p.v) + (size_t)kvh * 256 + ch * 16;
+    const bool pow2 = (P & (P - 1)) == 0;
+    const int pshift = __ffs(P) - 1;
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kNumStages;
+      if (k >= kNumStages && !mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err)) break;
+      const uint32_t dst0 = smem_u32(stages + slot * kStageBytes) + col + tl * 128;
+      const int t0 = c0 + k * ST + tl;
+#pragma unroll
+      for (int j = 0; j < ST / 8; ++j) {
+        const int t = t0 + 8 * j;
+        int pg = -1, slotp = 0;
+        if (t < kv_len) {
+          const int pi = pow2 ? (t >> pshift) : (t / P);
+          slotp = t - pi * P;
+          pg = bt_s[pi - pg0];
+        }
+        const bool ok = pg >= 0 && pg < p.num_pages;
+        const size_t row = ok ? ((size_t)pg * P + slotp) * tok_stride : 0;
+        const uint32_t n = ok ? 16u : 0u;   // positions past the sequence / bad pages: zeros
+        const uint32_t dst = dst0 + j * 1024;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(kcol + row),
+                     "r"(n)
+                     : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 2 * H),
+                     "l"(vcol + row), "r"(n)
+                     : "memory");
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                       smem_u32(&full[slot]))
+                   : "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  // Q tile (consumer warps): row rho = i*G + g of this KV head -> q[b, i, kvh*G + g, :]
+  for (int idx = threadIdx.x; idx < RT * 16; idx += 32 * kConsumerWarps) {
     const int r = idx >> 4, c = idx & 15;
     const int rho = rt * RT + r;
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -101,48 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *reinterpret_cast<uint4*>(qs + r * kQStride + c * 8) = v;
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer warp: block-table slice, then TMA stages
-    const int P = p.page_size;
-    const int pg0 = c0 / P;
-    const int npg = (c1 - 1) / P - pg0 + 1;
-    // entries past the table width (a caller error) read as -1: such tokens
-    // load as TMA out-of-bounds zeros instead of touching foreign memory
-    for (int i = lane; i < npg; i += 32)
-      bt_s[i] = (pg0 + i < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + pg0 + i] : -1;
-    __syncwarp();
-    if (lane == 0) {
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
-      for (int k = 0; k < nst; ++k) {
-        const int slot = k % kNumStages;
-        if (k >= kNumStages) {
-          if (!mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err)) break;
-        }
-        uint8_t* st = stages + slot * kStageBytes;
-        mbar_arrive_expect_tx(&full[slot], kStageBytes);
-        const int t0 = c0 + k * kStageTokens;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int t = t0 + 16 * g;
-          int y = -16;  // fully out of bounds: TMA fills zeros
-          if (t < kv_len) {
-            const int pg = bt_s[t / P - pg0];
-            if (pg >= 0 && pg < p.num_pages) y = pg * P + (t % P);
-          }
-          tma_load_3d(st + 0 * 8192 + g * 2048, &kmap, &full[slot], 0, kvh, y);
-          tma_load_3d(st + 1 * 8192 + g * 2048, &kmap, &full[slot], 64, kvh, y);
-          tma_load_3d(st + 2 * 8192 + g * 2048, &vmap, &full[slot], 0, kvh, y);
-          tma_load_3d(st + 3 * 8192 + g * 2048, &vmap, &full[slot], 64, kvh, y);
-        }
-      }
-    }
-    return;
-  }
-
-  // ---------------- consumer warps
+  // ---------------- consumer warps: every warp takes its 16-row group and its
+  // TS-token sub-block of EVERY stage, so a stage is released as soon as the
+  // eight warps finish their short slices of it
   const int rg = warp % NRG;
   const int tg = warp / NRG;
   const int r0 = lane >> 2;           // accumulator rows r0 and r0 + 8
@@ -152,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool v0 = rho0 < p.RG, v1 = rho1 < p.RG;
   const uint64_t w0 = v0 ? p.anc_mask[(size_t)b * p.R + rho0 / p.G] : 0ull;
   const uint64_t w1 = v1 ? p.anc_mask[(size_t)b * p.R + rho1 / p.G] : 0ull;
+  const int tsb = tg * TS;            // first token of this warp's sub-block
 
   const uint32_t q_base = smem_u32(qs);
   float o[16][4];
@@ -159,21 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
-  bool ok = true;
 
-  for (int k = tg; k < nst && ok; k += NTG) {
+  for (int k = 0; k < nst; ++k) {
     const int slot = k % kNumStages;
-    if (!mbar_wait(&full[slot], (k / kNumStages) & 1, p.err)) {
-      ok = false;
-      break;
-    }
+    if (!mbar_wait(&full[slot], (k / kNumStages) & 1, p.err)) break;
     const uint32_t st = smem_u32(stages + slot * kStageBytes);
-    const int tb = c0 + k * kStageTokens;
+    const int tb = c0 + k * ST + tsb;   // first cache position of the sub-block
 
-    // ---- S = Q K^T for 16 rows x 64 tokens
-    float sacc[8][4];
+    // ---- S = Q K^T for 16 rows x TS tokens
+    float sacc[NT][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+    for (int i = 0; i < NT; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t a[4];
@@ -183,12 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunk = 2 * ks + (m >> 1);
         ldmatrix_x4(a[0], a[1], a[2], a[3], q_base + row * (kQStride * 2) + chunk * 16);
       }
-      const uint32_t kb = st + (ks >> 2) * 8192;
+      const uint32_t kb = st + (ks >> 2) * H;
       const int cbase = (2 * ks) & 7;
 #pragma unroll
-      for (int ntp = 0; ntp < 4; ++ntp) {
+      for (int ntp = 0; ntp < NT / 2; ++ntp) {
         const int m = lane >> 3, r = lane & 7;
-        const int tok = 8 * (2 * ntp + (m >> 1)) + r;
+        const int tok = tsb + 8 * (2 * ntp + (m >> 1)) + r;
         const int chunk = cbase + (m & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(b0, b1, b2, b3, kb + tok * 128 + ((chunk ^ (tok & 7)) << 4));
@@ -198,10 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- scale, visibility mask, online softmax (log2 domain)
-    const bool need_mask = tb + kStageTokens > ctx;
+    const bool need_mask = tb + TS > ctx;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float x = sacc[nt][e] * p.scale_log2;
@@ -228,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float rs[2] = {0.f, 0.f};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float pe = fast_exp2(sacc[nt][e] - base[e >> 1]);
@@ -238,30 +286,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row maximum moved
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-
-    // ---- rows of V past the end of the sequence may hold stale cache
-    // contents; zero them so that 0 * garbage cannot produce NaN.
-    const uint32_t vb = st + 2 * 8192;
-    if (tb + kStageTokens > kv_len) {
-      const int first = max(kv_len - tb, 0);
-      for (int idx = lane; idx < (kStageTokens - first) * 16; idx += 32) {
-        const int tok = first + (idx >> 4), ch = idx & 15;
-        const uint32_t addr = vb + (ch >> 3) * 8192 + tok * 128 + ((ch & 7) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= alpha[0];
+        o[i][1] *= alpha[0];
+        o[i][2] *= alpha[1];
+        o[i][3] *= alpha[1];
       }
-      __syncwarp();
     }
 
-    // ---- O += P V
+    const uint32_t vb = st + 2 * H;
+
+    // ---- O += P V over the sub-block
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < TS / 16; ++j) {
       uint32_t a[4];
       a[0] = pack_bf16(sacc[2 * j][0], sacc[2 * j][1]);
       a[1] = pack_bf16(sacc[2 * j][2], sacc[2 * j][3]);
@@ -271,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int dp = 0; dp < 8; ++dp) {
         const int c = 2 * dp;
         const int m = lane >> 3, r = lane & 7;
-        const int tok = 16 * j + 8 * (m & 1) + r;
+        const int tok = tsb + 16 * j + 8 * (m & 1) + r;
         const int chunk = (c & 7) + (m >> 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(b0, b1, b2, b3,
-                          vb + (c >> 3) * 8192 + tok * 128 + ((chunk ^ (tok & 7)) << 4));
+                          vb + (c >> 3) * H + tok * 128 + ((chunk ^ (tok & 7)) << 4));
         mma_bf16_16816(o[c], a, b0, b1);
         mma_bf16_16816(o[c + 1], a, b2, b3);
       }
@@ -340,9 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ fp32 CUDA-core kernel
-// One warp per query row; lanes split the keys 32 at a time, each lane owns
-// D/32 output dimensions.  Used for fp32 caches (small shapes).
+// fp32 caches: 32-token K/V tiles staged through shared memory (coalesced
+// row loads through the block table, padded rows for conflict-free dot
+// products); one warp per query row, lane j scores token j of the tile,
+// lanes own D/32 output dimensions each.
+constexpr int kF32Tile = 32;
+
 __global__ void __launch_bounds__(128) attn_partial_f32(const AttnParams p) {
+  __shared__ float ks[kF32Tile][128 + 1];
+  __shared__ float vs[kF32Tile][128 + 1];
+  __shared__ float qsh[4][128];
   const int s = blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
@@ -355,25 +401,43 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const AttnParams p) {
   const int D = p.D;
   const int nd = D / 32;
   const int P = p.page_size;
-  for (int rho = warp; rho < p.RG; rho += 4) {
-    const int i = rho / p.G, g = rho % p.G;
-    const float* qrow = p.qf + (((size_t)b * p.R + i) * p.Hq + (size_t)kvh * p.G + g) * D;
-    const uint64_t w = p.anc_mask[(size_t)b * p.R + i];
+  // rows are processed four at a time (one per warp); every warp walks every tile
+  for (int rbase = 0; rbase < p.RG; rbase += 4) {
+    const int rho = rbase + warp;
+    const bool live = rho < p.RG;
+    const int i = live ? rho / p.G : 0, g = live ? rho % p.G : 0;
+    const uint64_t w = live ? p.anc_mask[(size_t)b * p.R + i] : 0ull;
+    if (live)
+      for (int d = lane; d < D; d += 32)
+        qsh[warp][d] = p.qf[(((size_t)b * p.R + i) * p.Hq + (size_t)kvh * p.G + g) * D + d];
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     float m_run = -INFINITY, l_run = 0.f;
-    for (int t0 = c0; t0 < c1; t0 += 32) {
+    for (int t0 = c0; t0 < c1; t0 += kF32Tile) {
+      __syncthreads();  // previous tile consumed
+      for (int idx = threadIdx.x; idx < kF32Tile * D; idx += 128) {
+        const int j = idx / D, d = idx % D;
+        const int t = t0 + j;
+        float kv = 0.f, vv = 0.f;
+        if (t < c1) {
+          const int page = (t / P < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + t / P] : -1;
+          if (page >= 0 && page < p.num_pages) {
+            const size_t roff = (((size_t)page * P + (t % P)) * p.Hkv + kvh) * D + d;
+            kv = p.kf[roff];
+            vv = p.vf[roff];
+          }
+        }
+        ks[j][d] = kv;
+        vs[j][d] = vv;
+      }
+      __syncthreads();
       const int t = t0 + lane;
       float x = -INFINITY;
-      size_t roff = 0;
-      if (t < c1) {
-        const int j = t - ctx;
-        const bool vis = (t < ctx) || (j < p.R && ((w >> j) & 1ull));
-        const int page = (t / P < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + t / P] : -1;
-        const bool pg_ok = page >= 0 && page < p.num_pages;
-        roff = pg_ok ? (((size_t)page * P + (t % P)) * p.Hkv + kvh) * D : 0;
-        if (vis && pg_ok) {
+      if (live && t < c1) {
+        const int jb = t - ctx;
+        const bool vis = (t < ctx) || (jb < p.R && ((w >> jb) & 1ull));
+        if (vis) {
           float dot = 0.f;
-          for (int d = 0; d < D; ++d) dot = fmaf(qrow[d], p.kf[roff + d], dot);
+          for (int d = 0; d < D; ++d) dot = fmaf(qsh[warp][d], ks[lane][d], dot);
           x = dot * p.scale_log2;
         }
       }
@@ -385,97 +449,104 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const AttnParams p) {
       l_run = l_run * alpha + warp_sum(pe);
       m_run = mnew;
       for (int c = 0; c < nd; ++c) o[c] *= alpha;
-      const int nvalid = min(32, c1 - t0);
+      const int nvalid = min(kF32Tile, c1 - t0);
       for (int jj = 0; jj < nvalid; ++jj) {
         const float pj = __shfl_sync(0xffffffffu, pe, jj);
-        const size_t rj = __shfl_sync(0xffffffffu, roff, jj);
-        if (pj != 0.f)
-          for (int c = 0; c < nd; ++c) o[c] = fmaf(pj, p.vf[rj + lane + 32 * c], o[c]);
+        for (int c = 0; c < nd; ++c) o[c] = fmaf(pj, vs[jj][lane + 32 * c], o[c]);
       }
     }
-    const size_t prow = (((size_t)b * p.Hkv + kvh) * p.RGpad + rho) * p.S + s;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    for (int c = 0; c < nd; ++c) p.o_part[prow * D + lane + 32 * c] = o[c] * inv;
-    if (lane == 0) p.lse_part[prow] = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+    if (live) {
+      const size_t prow = (((size_t)b * p.Hkv + kvh) * p.RGpad + rho) * p.S + s;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      for (int c = 0; c < nd; ++c) p.o_part[prow * D + lane + 32 * c] = o[c] * inv;
+      if (lane == 0) p.lse_part[prow] = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+    }
   }
 }
 
 // ------------------------------------------------------------------ LSE combine
 // out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M), one warp per output row.
+// Launched as a programmatic dependent of the partial pass: everything up to
+// griddepcontrol.wait overlaps the partial pass's tail.
 template <typename OutT>
 __global__ void __launch_bounds__(128) attn_combine(const AttnParams p, OutT* __restrict__ out,
                                                    float* __restrict__ lse_out) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int total = p.B * p.R * p.Hq;
-  if (gw >= total) return;
-  const int hq = gw % p.Hq;
-  const int i = (gw / p.Hq) % p.R;
-  const int b = gw / (p.Hq * p.R);
+  const bool live = gw < total;
+  const int hq = live ? gw % p.Hq : 0;
+  const int i = live ? (gw / p.Hq) % p.R : 0;
+  const int b = live ? gw / (p.Hq * p.R) : 0;
   const int kvh = hq / p.G, g = hq % p.G;
   const int rho = i * p.G + g;
-  const int kv_len = p.ctx_len[b] + p.R;
+  const int kv_len = live ? p.ctx_len[b] + p.R : 0;
   const int ns = min(p.S, (kv_len + p.chunk - 1) / p.chunk);
   const size_t prow0 = (((size_t)b * p.Hkv + kvh) * p.RGpad + rho) * p.S;
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.lse_part[prow0 + s]);
-  M = warp_max(M);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!live) return;
   const int D = p.D;
-  const int nv = D / 128 == 1 ? 1 : 0;  // D == 128: float4 per lane; D == 64: float2
+  const int per = D / 32;  // 4 (D = 128) or 2 (D = 64) floats per lane
+  float M = -INFINITY;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(&p.lse_part[prow0 + s]));
+  M = warp_max(M);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float L = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float ls = p.lse_part[prow0 + s];
-    const float e = (ls == -INFINITY) ? 0.f : fast_exp2(ls - M);
-    L += e;
-    const float* src = p.o_part + (prow0 + s) * D;
-    if (nv) {
-      const float4 v = *reinterpret_cast<const float4*>(src + 4 * lane);
-      acc[0] += e * v.x;
-      acc[1] += e * v.y;
-      acc[2] += e * v.z;
-      acc[3] += e * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src + 2 * lane);
-      acc[0] += e * v.x;
-      acc[1] += e * v.y;
+  constexpr int kBatch = 8;
+  for (int s0 = 0; s0 < ns; s0 += kBatch) {
+    float ls[kBatch];
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {  // independent loads, all in flight together
+      const int s = s0 + j;
+      ls[j] = s < ns ? __ldcg(&p.lse_part[prow0 + s]) : -INFINITY;
+      const float* src = p.o_part + (prow0 + min(s, ns - 1)) * D + per * lane;
+      v[j] = per == 4 ? __ldcg(reinterpret_cast<const float4*>(src))
+                      : make_float4(__ldcg(src), __ldcg(src + 1), 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const float e = (ls[j] == -INFINITY) ? 0.f : fast_exp2(ls[j] - M);
+      L += e;
+      acc[0] += e * v[j].x;
+      acc[1] += e * v[j].y;
+      acc[2] += e * v[j].z;
+      acc[3] += e * v[j].w;
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   OutT* dst = out + (((size_t)b * p.R + i) * p.Hq + hq) * D;
-  const int per = nv ? 4 : 2;
   for (int c = 0; c < per; ++c) {
-    const float v = acc[c] * inv;
+    const float val = acc[c] * inv;
     if constexpr (sizeof(OutT) == 2)
-      dst[per * lane + c] = __float2bfloat16_rn(v);
+      dst[per * lane + c] = __float2bfloat16_rn(val);
     else
-      dst[per * lane + c] = v;
+      dst[per * lane + c] = val;
   }
   if (lse_out && lane == 0)
     lse_out[((size_t)b * p.R + i) * p.Hq + hq] =
         (L > 0.f) ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
-// ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
+template <typename OutT>
+spec_status launch_combine(const AttnParams& prm, OutT* out, float* lse_out, cudaStream_t st) {
+  const int rows = prm.B * prm.R * prm.Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows * 32 + 127) / 128, 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_combine<OutT>, prm, out, lse_out) != cudaSuccess)
+    return SPEC_ECUDA;
+  return launch_status();
 }
 
+// ------------------------------------------------------------------ host side
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -499,7 +570,7 @@ bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_page
   pl->G = Hq / Hkv;
   pl->RG = R * pl->G;
   if (bf16) {
-    pl->NRG = pl->RG <= 16 ? 1 : pl->RG <= 32 ? 2 : pl->RG <= 64 ? 4 : 8;
+    pl->NRG = pl->RG <= 32 ? 2 : pl->RG <= 64 ? 4 : 8;
     pl->RT = 16 * pl->NRG;
     pl->row_tiles = (pl->RG + pl->RT - 1) / pl->RT;
     pl->RGpad = pl->row_tiles * pl->RT;
@@ -511,21 +582,22 @@ bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_page
   }
   const long long max_kv = (long long)max_pages * page_size;
   const int units = B * Hkv * pl->row_tiles;
+  const int g = (bf16 && pl->NRG == 2) ? 128 : kStageTokens;  // stage size of the kernel
   int chunk;
   if (num_splits > 0) {
     chunk = (int)((max_kv + num_splits - 1) / num_splits);
-    chunk = chunk >= 128 ? chunk / kStageTokens * kStageTokens : round_up(chunk, kStageTokens);
+    chunk = chunk >= 2 * g ? chunk / g * g : round_up(chunk, g);
   } else {
     const int sms = num_sms();
     if (units >= sms) {
       chunk = 2048;
     } else {
       const int S = std::max(1, sms / units);
-      chunk = round_up((int)((max_kv + S - 1) / S), kStageTokens);
+      chunk = round_up((int)((max_kv + S - 1) / S), g);
       if (chunk > 2048) chunk = 2048;
     }
   }
-  chunk = std::max(kStageTokens, std::min(chunk, kMaxChunk));
+  chunk = std::max(g, std::min(chunk, kMaxChunk));
   pl->chunk = chunk;
   pl->S = (int)((max_kv + chunk - 1) / chunk);
   return true;
@@ -541,15 +613,14 @@ size_t ws_layout(const Plan& pl, int B, int Hkv, int D, size_t* off_o, size_t* o
   return off;
 }
 
-size_t smem_bytes_bf16(int NRG) {
-  return 1024 + (size_t)kNumStages * kStageBytes + (size_t)16 * NRG * kQStride * 2 +
-         (kMaxChunk / 16 + 8) * 4 + 2 * kNumStages * 8;
+size_t smem_bytes_bf16(int NRG, int stages, int stage_tok) {
+  return 1024 + (size_t)stages * stage_tok * 512 + (size_t)16 * NRG * kQStride * 2 +
+         (kMaxChunk / 16 + 8) * 4 + 2 * stages * 8;
 }
 
 template <int NRG>
-spec_status launch_bf16(const CUtensorMap& km, const CUtensorMap& vm, const AttnParams& prm,
-                        const Plan& pl, cudaStream_t st) {
-  const size_t smem = smem_bytes_bf16(NRG);
+spec_status launch_bf16(const AttnParams& prm, const Plan& pl, cudaStream_t st) {
+  const size_t smem = smem_bytes_bf16(NRG, stages_for<NRG>(), stage_tokens<NRG>());
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_partial_bf16<NRG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -557,8 +628,8 @@ spec_status launch_bf16(const CUtensorMap& km, const CUtensorMap& vm, const Attn
       return SPEC_ECUDA;
     attr_set = true;
   }
-  dim3 grid(pl.S, prm.Hkv * pl.row_tiles, prm.B);
-  attn_partial_bf16<NRG><<<grid, kThreads, smem, st>>>(km, vm, prm);
+  dim3 grid(prm.Hkv * pl.row_tiles, pl.S, prm.B);
+  attn_partial_bf16<NRG><<<grid, kThreads, smem, st>>>(prm);
   return launch_status();
 }
 
@@ -623,6 +694,8 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   prm.qf = static_cast<const float*>(q);
   prm.kf = static_cast<const float*>(k_cache);
   prm.vf = static_cast<const float*>(v_cache);
+  prm.k = k_cache;
+  prm.v = v_cache;
   prm.block_table = block_table;
   prm.ctx_len = ctx_len;
   prm.anc_mask = anc_mask;
@@ -650,27 +723,10 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   if (phase & kPartials) {
     spec_status rc;
     if (bf16) {
-      EncodeTiledFn enc = get_encode();
-      if (!enc) return SPEC_ECUDA;
-      CUtensorMap km, vm;
-      const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv,
-                                  (cuuint64_t)num_pages * page_size};
-      const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-      const cuuint32_t box[3] = {64, 1, 16};
-      const cuuint32_t estr[3] = {1, 1, 1};
-      if (enc(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k_cache), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return SPEC_ECUDA;
-      if (enc(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v_cache), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return SPEC_ECUDA;
       switch (pl.NRG) {
-        case 1: rc = launch_bf16<1>(km, vm, prm, pl, st); break;
-        case 2: rc = launch_bf16<2>(km, vm, prm, pl, st); break;
-        case 4: rc = launch_bf16<4>(km, vm, prm, pl, st); break;
-        default: rc = launch_bf16<8>(km, vm, prm, pl, st); break;
+        case 2: rc = launch_bf16<2>(prm, pl, st); break;
+        case 4: rc = launch_bf16<4>(prm, pl, st); break;
+        default: rc = launch_bf16<8>(prm, pl, st); break;
       }
     } else {
       dim3 grid(pl.S, Hkv, B);
@@ -680,14 +736,8 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
     if (rc != SPEC_OK) return rc;
   }
   if (phase & kCombine) {
-    const int rows = B * R * Hq;
-    const int blocks = (rows * 32 + 127) / 128;
-    if (bf16)
-      attn_combine<__nv_bfloat16><<<blocks, 128, 0, st>>>(prm, static_cast<__nv_bfloat16*>(out),
-                                                          lse_out);
-    else
-      attn_combine<float><<<blocks, 128, 0, st>>>(prm, static_cast<float*>(out), lse_out);
-    return launch_status();
+    if (bf16) return launch_combine<__nv_bfloat16>(prm, static_cast<__nv_bfloat16*>(out), lse_out, st);
+    return launch_combine<float>(prm, static_cast<float*>(out), lse_out, st);
   }
   return SPEC_OK;
 }

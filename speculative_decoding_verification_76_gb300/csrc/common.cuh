@@ -72,6 +72,8 @@ SPEC_DEV uint64_t global_ns() {
 // complete within SPEC_WAIT_NS.
 SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
+  // once any wait of this launch has given up, later waits give up at once
+  if (err && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int it = 0; it < 256; ++it)
@@ -105,6 +107,13 @@ SPEC_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64
           "r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Warm [gsrc, gsrc + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+SPEC_DEV void prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)),
+               "r"(bytes)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- clusters

@@ -13,20 +13,22 @@
 //
 // GB300 design.  One thread-block cluster (up to 8 CTAs) per target row
 // holds that row in distributed shared memory: each CTA bulk-copies (TMA)
-// one slice of the vocabulary once and every later pass -- max, normaliser,
-// the top-k / top-p radix selection, the p output -- runs from shared
-// memory, with cluster-wide reductions over DSMEM.  Rows are independent,
-// so all B*R rows run at once.  The cluster that finishes a sequence's last
-// row (an atomic counter per sequence) runs the left-to-right walk and then
-// the correction / bonus draw: a cluster-wide prefix sum over the drawn row
-// in ascending id order.  The draft-tree walk keeps the running residual p'
-// dense in the same distributed shared memory.
+// one slice of the vocabulary once; max, exp values, normaliser, the
+// top-k / top-p cut and the draws all run from shared memory, with
+// cluster-wide reductions gathered by one warp over DSMEM.  Every row
+// computes its own outcome independently (its draft test, and its
+// correction draw if it rejects; the last row's bonus draw; for a tree node
+// the first accepted child under the running residual, or its final draw),
+// so all B*R rows run at once and nothing waits on a serial walk.  The
+// cluster that finishes a sequence's last row assembles the outcomes.
 //
 // Numerics: exp((l - m)/T) is evaluated with the difference and quotient
-// carried in two floats, so p matches a float64 evaluation to ~3e-7
-// relative; normalisers use per-thread compensated sums and a float64 tree;
-// top-p masses are accumulated in 2^-40 fixed point so the selection is
-// deterministic.
+// carried in two floats (p matches a float64 evaluation to ~3e-7 relative);
+// sums are per-thread compensated and combined as float pairs in a fixed
+// order, so results are deterministic.  top-k / top-p: a 1/16-nat histogram
+// (below the row maximum) locates the crossing bin, its members are sorted
+// exactly by (logit desc, id asc); an exact radix selection is the fallback
+// for crossing bins too populous to sort.
 #include <algorithm>
 #include <climits>
 
@@ -39,16 +41,15 @@ constexpr int kSW = kST / 32;
 constexpr int kMaxCS = 8;
 constexpr int kMaxN = 64;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr size_t kMaxSliceBytes = 200 * 1024;
+constexpr int kCandMax = 1024;                 // sortable members of one crossing bin
+constexpr size_t kMaxSliceBytes = 84 * 1024;   // per CTA: logits + exp slices, each this size
 
-struct RowStat {
-  float m;
-  float Z;
-  uint32_t tau;
-  int32_t tie_cut;
-  int32_t argmax;
-  int32_t flags;
-  int32_t pad[2];
+// Outcome of one target row, written by its cluster.
+struct Outcome {
+  int32_t accept;  // chain: 1 if the row's draft is accepted; tree: accepted child or -1
+  int32_t token;   // correction / bonus / final token of this row (-1 if none)
+  int32_t status;  // SPEC_SEQ_* bits raised by this row
+  int32_t flags;   // 1 if the row's logits are not finite
 };
 
 struct SP {
@@ -61,8 +62,8 @@ struct SP {
   float T, invT;
   int top_k;
   float top_p;
-  int greedy, eos, tree, bulk;
-  RowStat* stats;
+  int greedy, eos, tree, bulk, qbulk;
+  Outcome* outcomes;
   int32_t* seq_count;
   int32_t* err;
   int32_t* acc_len;
@@ -76,26 +77,33 @@ struct alignas(16) Slot {
   unsigned long long a, b;
 };
 
+struct DF {  // hi + lo, |lo| <= ulp(hi)/2
+  float hi, lo;
+};
+
 struct Shared {
-  double red_d[kSW];
   float red_f[kSW];
   int red_i[kSW];
-  uint32_t red_u[kSW];
-  unsigned long long red_ull[kSW];
+  DF red_df[kSW];
   Slot slots[4];
-  unsigned long long hmass[2][256];
-  uint32_t hcnt[2][256];
-  unsigned long long tot_mass[256];
-  uint32_t tot_cnt[256];
+  Slot gath[kMaxCS];
+  uint32_t hcnt[256];
+  float hmass[256];
+  uint32_t tcnt[256];
+  float tmass[256];
+  uint32_t rcnt[2][256];
+  unsigned long long rmass[2][256];
+  unsigned long long rtmass[256];
+  uint32_t rtcnt[256];
   int bi[8];
-  float bf[8];
-  uint32_t bu[8];
-  unsigned long long bull[2];
+  DF bdf[2];
   int par[kMaxN];
   int tok[kMaxN];
+  Outcome outs[kMaxN];
   uint64_t bar;
 };
 
+// ---------------------------------------------------------------- scalar helpers
 // order-preserving key: larger float -> larger key; -0 and +0 share a key
 SPEC_DEV uint32_t okey(float x) {
   uint32_t u = __float_as_uint(x);
@@ -121,21 +129,53 @@ SPEC_DEV bool is_kept(uint32_t key, int id, uint32_t tau, int tie) {
   return key > tau || (key == tau && id <= tie);
 }
 
+SPEC_DEV DF df_norm(float a, float b) {  // fast two-sum, |a| >= |b| or a == 0
+  const float s = a + b;
+  return DF{s, b - (s - a)};
+}
+
+SPEC_DEV DF df_add(DF a, DF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb) + a.lo + b.lo;
+  return df_norm(s, e);
+}
+
+struct Kahan {
+  float s = 0.f, c = 0.f;
+  SPEC_DEV void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+  SPEC_DEV DF df() const { return df_norm(s, -c); }
+};
+
+SPEC_DEV double df_d(DF a) { return (double)a.hi + (double)a.lo; }
+
 // ---------------------------------------------------------------- block reductions
-SPEC_DEV double block_sum_d(double v, Shared& sh) {
+SPEC_DEV DF block_sum_df(DF v, Shared& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  if (lane == 0) sh.red_d[w] = v;
+  for (int o = 16; o > 0; o >>= 1)
+    v = df_add(v, DF{__shfl_xor_sync(kFull, v.hi, o), __shfl_xor_sync(kFull, v.lo, o)});
+  if (lane == 0) sh.red_df[w] = v;
   __syncthreads();
-  double t = 0.0;
+  if (w == 0) {
+    DF x = lane < kSW ? sh.red_df[lane] : DF{0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < kSW; ++i) t += sh.red_d[i];
+    for (int o = 16; o > 0; o >>= 1)
+      x = df_add(x, DF{__shfl_xor_sync(kFull, x.hi, o), __shfl_xor_sync(kFull, x.lo, o)});
+    if (lane == 0) sh.bdf[0] = x;
+  }
+  __syncthreads();
+  const DF t = sh.bdf[0];
   __syncthreads();
   return t;
 }
 
-// (max value, lowest id among maxima); non-finite flag OR-ed
+// (max value, lowest id among maxima)
 SPEC_DEV void block_max_arg(float& v, int& id, Shared& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -185,8 +225,8 @@ SPEC_DEV int block_min_i(int v, Shared& sh) {
   return t;
 }
 
-// exclusive scan of one float per thread (fixed order); returns the
-// exclusive prefix and writes the block total to *total.
+// exclusive scan of one float per thread (fixed order); *total = block total
+// computed the way the last thread's running value is.
 SPEC_DEV float block_excl_scan_f(float v, float* total, Shared& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   float incl = v;
@@ -201,7 +241,6 @@ SPEC_DEV float block_excl_scan_f(float v, float* total, Shared& sh) {
   for (int i = 0; i < w; ++i) base += sh.red_f[i];
   const float excl = base + (incl - v);
   __syncthreads();
-  // total computed exactly the way the last element's running value is
   if (threadIdx.x == kST - 1) sh.red_f[0] = excl + v;
   __syncthreads();
   *total = sh.red_f[0];
@@ -230,61 +269,52 @@ SPEC_DEV int block_excl_scan_i(int v, int* total, Shared& sh) {
 }
 
 // ---------------------------------------------------------------- cluster exchange
-// Every CTA posts one Slot; afterwards thread-local copies of all CS slots
-// (rank order) are available to warp 0 lanes < CS.  Slots rotate over four
-// buffers so that a slot is never rewritten before every reader has passed
+// Every CTA posts one Slot; warp 0 fetches all CS slots (lane r <- rank r)
+// into sh.gath, which every thread then reads locally.  Posting slots rotate
+// over four buffers so a slot is never rewritten before every reader is past
 // the next cluster barrier.
-SPEC_DEV Slot cluster_post_get(Slot mine, int& ph, Shared& sh, uint32_t rank_to_read) {
+SPEC_DEV void cluster_allgather(Slot mine, int CS, int& ph, Shared& sh) {
   Slot* s = &sh.slots[ph & 3];
   if (threadIdx.x == 0) *s = mine;
   cluster_sync();
-  Slot r;
-  r.a = dsmem_ld_u64(&s->a, rank_to_read);
-  r.b = dsmem_ld_u64(&s->b, rank_to_read);
+  if ((int)threadIdx.x < CS) {
+    Slot r;
+    r.a = dsmem_ld_u64(&s->a, threadIdx.x);
+    r.b = dsmem_ld_u64(&s->b, threadIdx.x);
+    sh.gath[threadIdx.x] = r;
+  }
+  __syncthreads();
   ++ph;
-  return r;
 }
 
-SPEC_DEV double cluster_sum_d(double v, int CS, int& ph, Shared& sh) {
-  Slot mine{(unsigned long long)__double_as_longlong(v), 0ull};
-  double t = 0.0;
-  // every thread reads every rank (CS <= 8 DSMEM loads), in rank order
-  Slot* s = &sh.slots[ph & 3];
-  if (threadIdx.x == 0) *s = mine;
-  cluster_sync();
-  for (int r = 0; r < CS; ++r) t += __longlong_as_double((long long)dsmem_ld_u64(&s->a, r));
-  ++ph;
+SPEC_DEV Slot cluster_from(Slot mine, int src, int CS, int& ph, Shared& sh) {
+  cluster_allgather(mine, CS, ph, sh);
+  return sh.gath[src];
+}
+
+SPEC_DEV Slot slot_df(DF v) {
+  return Slot{(unsigned long long)__float_as_uint(v.hi), (unsigned long long)__float_as_uint(v.lo)};
+}
+
+SPEC_DEV DF cluster_sum_df(DF v, int CS, int& ph, Shared& sh) {
+  cluster_allgather(slot_df(v), CS, ph, sh);
+  DF t{0.f, 0.f};
+  for (int r = 0; r < CS; ++r)
+    t = df_add(t, DF{__uint_as_float((uint32_t)sh.gath[r].a),
+                     __uint_as_float((uint32_t)sh.gath[r].b)});
   return t;
 }
 
-SPEC_DEV unsigned long long cluster_sum_u64(unsigned long long v, int CS, int& ph, Shared& sh) {
-  Slot* s = &sh.slots[ph & 3];
-  if (threadIdx.x == 0) s->a = v;
-  cluster_sync();
-  unsigned long long t = 0;
-  for (int r = 0; r < CS; ++r) t += dsmem_ld_u64(&s->a, r);
-  ++ph;
-  return t;
-}
-
-// value of CTA `src` (posted by every CTA; only src's value is used)
-SPEC_DEV Slot cluster_from(Slot mine, int src, int& ph, Shared& sh) {
-  return cluster_post_get(mine, ph, sh, (uint32_t)src);
-}
-
-// ---------------------------------------------------------------- helpers on the slice
+// ---------------------------------------------------------------- the slice
 struct Slice {
   float* buf;  // shared memory, n floats
   int lo, n;
 };
 
-// Load logits row into the slice buffer (TMA bulk copy when aligned).
+// Load a row slice into shared memory (TMA bulk copy when aligned).
 SPEC_DEV void load_row(const SP& p, const float* row, Slice& sl, Shared& sh, uint32_t& bar_phase) {
   __syncthreads();  // every reader of the previous contents is done
-  if (sl.n <= 0) {
-    __syncthreads();
-    return;
-  }
+  if (sl.n <= 0) return;
   if (p.bulk) {
     if (threadIdx.x == 0) {
       fence_proxy_async();  // order earlier generic writes before the async copy
@@ -299,28 +329,400 @@ SPEC_DEV void load_row(const SP& p, const float* row, Slice& sl, Shared& sh, uin
   __syncthreads();
 }
 
+// coarse bin of a logit: 1/16 nat below the row maximum, 255 = beyond 16 nats
+SPEC_DEV int coarse_bin(float l, float m, float scale16) {
+  const float d = (m - l) * scale16;  // monotone non-increasing in l
+  return d < 255.f ? (int)d : 255;
+}
+
+// Deterministic cluster sum of E over the elements with pred(k).
+template <class Pred>
+SPEC_DEV DF cluster_masked_sum(const Slice& sl, const float* E, Pred pred, int CS, int& ph,
+                               Shared& sh) {
+  Kahan acc;
+  for (int k = threadIdx.x; k < sl.n; k += kST)
+    if (pred(k)) acc.add(E[k]);
+  return cluster_sum_df(block_sum_df(acc.df(), sh), CS, ph, sh);
+}
+
+// First index d in [0, n) (n <= 256) where the running sum of val[0..d]
+// reaches target; -1 if none.  Warp 0 scans 8 bins per lane; the result is
+// broadcast to the block.
+template <class T>
+SPEC_DEV int first_reaching(const T* val, int n, double target, Shared& sh) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    double ls = 0.0;
+    for (int j = 0; j < 8; ++j)
+      if (8 * lane + j < n) ls += (double)val[8 * lane + j];
+    double incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(kFull, incl >= target);
+    int res = -1;
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      if (lane == L) {
+        double cum = incl - ls;
+        for (int j = 0; j < 8; ++j) {
+          const int d = 8 * L + j;
+          if (d >= n) break;
+          cum += (double)val[d];
+          if (cum >= target) {
+            res = d;
+            break;
+          }
+        }
+      }
+      res = __shfl_sync(kFull, res, L);
+    }
+    if (lane == 0) sh.bi[2] = res;
+  }
+  __syncthreads();
+  const int r = sh.bi[2];
+  __syncthreads();
+  return r;
+}
+
+// ---------------------------------------------------------------- crossing-bin sort
+SPEC_DEV uint64_t cand_of(float l, int id) {
+  return ((uint64_t)okey(l) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)id);
+}
+SPEC_DEV uint32_t cand_key(uint64_t c) { return (uint32_t)(c >> 32); }
+SPEC_DEV int cand_id(uint64_t c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
+
+struct Scratch {
+  uint64_t *cand, *gk, *sk;
+  float *candE, *ge, *se;
+};
+
+struct Sorted {
+  uint64_t* key;  // CTA 0: members sorted by (logit desc, id asc)
+  float* E;       // their exp values, same order
+  int n;
+};
+
+// Gather the elements with pred(k) (with their exp values) from every CTA
+// into CTA 0 and rank-sort them there.  The caller guarantees the cluster
+// count is <= kCandMax.  Same n in every CTA; keys valid in CTA 0 only.
+template <class Pred>
+SPEC_DEV Sorted gather_sort(const Slice& sl, const float* E, const Scratch& sc, Pred pred, int rank,
+                            int CS, int& ph, Shared& sh) {
+  if (threadIdx.x == 0) sh.bi[1] = 0;
+  __syncthreads();
+  for (int k = threadIdx.x; k < sl.n; k += kST) {
+    if (pred(k)) {
+      const int slot = atomicAdd(&sh.bi[1], 1);
+      if (slot < kCandMax) {
+        sc.cand[slot] = cand_of(sl.buf[k], sl.lo + k);
+        sc.candE[slot] = E[k];
+      }
+    }
+  }
+  __syncthreads();
+  const int mine = min(sh.bi[1], kCandMax);
+  cluster_allgather(Slot{(unsigned long long)mine, 0ull}, CS, ph, sh);
+  int cnt[kMaxCS];
+  int total = 0;
+  for (int r = 0; r < CS; ++r) {
+    cnt[r] = (int)sh.gath[r].a;
+    total += cnt[r];
+  }
+  total = min(total, kCandMax);
+  if (rank == 0) {
+    int off = 0;
+    for (int r = 0; r < CS; ++r) {
+      for (int j = threadIdx.x; j < cnt[r] && off + j < kCandMax; j += kST) {
+        sc.gk[off + j] = dsmem_ld_u64(&sc.cand[j], r);
+        sc.ge[off + j] = dsmem_ld_f32(&sc.candE[j], r);
+      }
+      off += cnt[r];
+    }
+    __syncthreads();
+    // rank sort: keys are distinct (ids are), rank = number of larger keys
+    for (int i = threadIdx.x; i < total; i += kST) {
+      const uint64_t c = sc.gk[i];
+      int rk = 0;
+      for (int j = 0; j < total; ++j) rk += sc.gk[j] > c ? 1 : 0;
+      sc.sk[rk] = c;
+      sc.se[rk] = sc.ge[i];
+    }
+    __syncthreads();
+  }
+  cluster_sync();  // other CTAs' candidate lists stay intact until CTA 0 has copied them
+  return Sorted{sc.sk, sc.se, total};
+}
+
+// In CTA 0: the first sorted index j whose base + sum(E[0..j]) reaches thr
+// (float-pair sums, fixed order), with that running sum; (-1, 0) if none.
+SPEC_DEV void sorted_crossing(const Sorted& so, DF base, double thr, int* idx, DF* at, Shared& sh) {
+  const int per = (so.n + kST - 1) / kST;
+  const int s0 = min((int)threadIdx.x * per, so.n), s1 = min(s0 + per, so.n);
+  DF run{0.f, 0.f};
+  for (int j = s0; j < s1; ++j) run = df_add(run, DF{so.E[j], 0.f});
+  // inclusive scan over the lanes, then over the warps, in a fixed order
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  DF incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF t = DF{__shfl_up_sync(kFull, incl.hi, o), __shfl_up_sync(kFull, incl.lo, o)};
+    if (lane >= o) incl = df_add(t, incl);
+  }
+  const DF lanes_before = DF{__shfl_up_sync(kFull, incl.hi, 1), __shfl_up_sync(kFull, incl.lo, 1)};
+  if (lane == 31) sh.red_df[w] = incl;
+  __syncthreads();
+  DF excl = base;
+  for (int i = 0; i < w; ++i) excl = df_add(excl, sh.red_df[i]);
+  if (lane > 0) excl = df_add(excl, lanes_before);
+  __syncthreads();
+  int found = INT_MAX;
+  DF val{0.f, 0.f};
+  if (df_d(df_add(excl, run)) >= thr) {
+    DF acc = excl;
+    for (int j = s0; j < s1; ++j) {
+      acc = df_add(acc, DF{so.E[j], 0.f});
+      if (df_d(acc) >= thr) {
+        found = j;
+        val = acc;
+        break;
+      }
+    }
+  }
+  const int f = block_min_i(found, sh);
+  if (found == f && f != INT_MAX) sh.bdf[1] = val;
+  __syncthreads();
+  *idx = (f == INT_MAX) ? -1 : f;
+  *at = (f == INT_MAX) ? DF{0.f, 0.f} : sh.bdf[1];
+  __syncthreads();
+}
+
+// In CTA 0: float-pair sum (fixed order) of the first n sorted exp values.
+SPEC_DEV DF sorted_head_sum(const Sorted& so, int n, Shared& sh) {
+  const int per = (n + kST - 1) / kST;
+  const int s0 = min((int)threadIdx.x * per, n), s1 = min(s0 + per, n);
+  DF run{0.f, 0.f};
+  for (int j = s0; j < s1; ++j) run = df_add(run, DF{so.E[j], 0.f});
+  return block_sum_df(run, sh);
+}
+
+struct Trunc {
+  uint32_t tau;
+  int tie;
+  DF Z;
+  bool ok;
+};
+
+// Top-k then top-p by coarse bins + an exact sort of the crossing bin.
+// ok = false when a crossing bin is too populous (the caller falls back to
+// the exact radix selection).
+SPEC_DEV Trunc truncate_fast(const SP& p, const Slice& sl, const float* E, const Scratch& sc,
+                             float m, DF Zall, int rank, int CS, int& ph, Shared& sh) {
+  Trunc tr{0u, INT_MAX, Zall, true};
+  const float s16 = p.invT * 16.f;
+  for (int d = threadIdx.x; d < 256; d += kST) {
+    sh.hcnt[d] = 0u;
+    sh.hmass[d] = 0.f;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < sl.n; k += kST) {
+    const int bn = coarse_bin(sl.buf[k], m, s16);
+    if (bn < 255) {
+      atomicAdd(&sh.hcnt[bn], 1u);
+      atomicAdd(&sh.hmass[bn], E[k]);
+    }
+  }
+  __syncthreads();
+  cluster_sync();
+  // cluster totals: thread d sums bin d over the ranks
+  for (int d = threadIdx.x; d < 256; d += kST) {
+    uint32_t c = 0;
+    float mm = 0.f;
+    for (int r = 0; r < CS; ++r) {
+      c += dsmem_ld_u32(&sh.hcnt[d], r);
+      mm += dsmem_ld_f32(&sh.hmass[d], r);
+    }
+    sh.tcnt[d] = c;
+    sh.tmass[d] = mm;
+  }
+  __syncthreads();
+  int bk = 254;  // last bin (partly) kept by top-k
+  if (p.top_k > 0 && p.top_k < p.V) {
+    const int bsel = first_reaching(sh.tcnt, 255, (double)p.top_k, sh);
+    if (bsel < 0 || sh.tcnt[bsel] > (uint32_t)kCandMax) {
+      tr.ok = false;
+      return tr;
+    }
+    uint32_t above_cnt = 0;
+    for (int d = 0; d < bsel; ++d) above_cnt += sh.tcnt[d];
+    const int need = p.top_k - (int)above_cnt;
+    const DF above = cluster_masked_sum(
+        sl, E, [&](int k) { return coarse_bin(sl.buf[k], m, s16) < bsel; }, CS, ph, sh);
+    const Sorted so = gather_sort(
+        sl, E, sc, [&](int k) { return coarse_bin(sl.buf[k], m, s16) == bsel; }, rank, CS, ph, sh);
+    const int nn = min(need, so.n);
+    Slot mine{0ull, 0ull};
+    if (rank == 0) {
+      const DF part = sorted_head_sum(so, nn, sh);
+      if (threadIdx.x == 0) mine = Slot{so.key[nn - 1], slot_df(part).a | (slot_df(part).b << 32)};
+    }
+    const Slot o = cluster_from(mine, 0, CS, ph, sh);
+    const DF part = DF{__uint_as_float((uint32_t)o.b), __uint_as_float((uint32_t)(o.b >> 32))};
+    tr.tau = cand_key(o.a);
+    tr.tie = cand_id(o.a);
+    tr.Z = df_add(above, part);
+    bk = bsel;
+  }
+  if (p.top_p > 0.f && p.top_p < 1.f) {
+    const double thr = (double)p.top_p * df_d(tr.Z);
+    const uint32_t tk = tr.tau;
+    const int tc = tr.tie;
+    int bp = first_reaching(sh.tmass, bk + 1, thr, sh);
+    if (bp < 0) bp = bk;
+    for (int attempt = 0; attempt < 6; ++attempt) {
+      if (bp < 0 || bp > bk || sh.tcnt[bp] > (uint32_t)kCandMax) break;
+      const int bsel = bp;
+      const DF above = cluster_masked_sum(
+          sl, E,
+          [&](int k) {
+            const float l = sl.buf[k];
+            return coarse_bin(l, m, s16) < bsel && is_kept(okey(l), sl.lo + k, tk, tc);
+          },
+          CS, ph, sh);
+      if (df_d(above) >= thr) {  // the crossing lies in an earlier bin
+        --bp;
+        continue;
+      }
+      const Sorted so = gather_sort(
+          sl, E, sc,
+          [&](int k) {
+            const float l = sl.buf[k];
+            return coarse_bin(l, m, s16) == bsel && is_kept(okey(l), sl.lo + k, tk, tc);
+          },
+          rank, CS, ph, sh);
+      Slot mine{~0ull, 0ull};
+      if (rank == 0) {
+        int idx;
+        DF at;
+        sorted_crossing(so, above, thr, &idx, &at, sh);
+        if (threadIdx.x == 0 && idx >= 0)
+          mine = Slot{so.key[idx], slot_df(at).a | (slot_df(at).b << 32)};
+      }
+      const Slot o = cluster_from(mine, 0, CS, ph, sh);
+      if (o.a == ~0ull) {  // not in this bin: move on to the next one
+        ++bp;
+        continue;
+      }
+      tr.tau = cand_key(o.a);
+      tr.tie = cand_id(o.a);
+      tr.Z = DF{__uint_as_float((uint32_t)o.b), __uint_as_float((uint32_t)(o.b >> 32))};
+      return tr;
+    }
+    tr.ok = false;
+  }
+  return tr;
+}
+
+// ---------------------------------------------------------------- exact radix fallback
+// Radix selection, most significant digit first, of the position in
+// (key desc, id asc) order where the running weight reaches the target.
+// Weight = 1 per element (top-k) or its 2^-40 fixed-point mass (top-p).
+struct Sel {
+  uint32_t tau;
+  unsigned long long above, at_weight, target;
+  uint32_t at_count;
+};
+
+template <class Keep, class Weight>
+SPEC_DEV Sel radix_select(const Slice& sl, bool target_is_fraction, double frac,
+                          unsigned long long target_abs, Keep keep, Weight weight, int CS, int& ph,
+                          Shared& sh) {
+  uint32_t prefix = 0, pmask = 0;
+  unsigned long long above = 0, target = target_abs;
+  Sel out{};
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    const int h = pass & 1;
+    for (int i = threadIdx.x; i < 256; i += kST) {
+      sh.rmass[h][i] = 0ull;
+      sh.rcnt[h][i] = 0u;
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < sl.n; k += kST) {
+      const uint32_t key = okey(sl.buf[k]);
+      if ((key & pmask) == prefix && keep(k, key)) {
+        const uint32_t digit = (key >> shift) & 255u;
+        atomicAdd(&sh.rcnt[h][digit], 1u);
+        atomicAdd(&sh.rmass[h][digit], weight(k));
+      }
+    }
+    __syncthreads();
+    cluster_sync();
+    for (int d = threadIdx.x; d < 256; d += kST) {
+      unsigned long long mm = 0;
+      uint32_t c = 0;
+      for (int r = 0; r < CS; ++r) {
+        mm += dsmem_ld_u64(&sh.rmass[h][d], r);
+        c += dsmem_ld_u32(&sh.rcnt[h][d], r);
+      }
+      sh.rtmass[255 - d] = mm;  // descending digit order
+      sh.rtcnt[255 - d] = c;
+    }
+    __syncthreads();
+    if (pass == 0 && target_is_fraction) {
+      unsigned long long tot = 0;
+      for (int d = 0; d < 256; ++d) tot += sh.rtmass[d];
+      const double thr = ceil(frac * (double)tot);
+      target = thr < 1.0 ? 1ull : (unsigned long long)thr;
+      if (target > tot) target = tot;
+    }
+    // first descending digit whose running weight reaches target - above
+    const unsigned long long need = target - above;
+    unsigned long long cum = 0;
+    int sel = 255;
+    for (int d = 0; d < 256; ++d) {  // every thread, identical result
+      if (cum + sh.rtmass[d] >= need) {
+        sel = d;
+        break;
+      }
+      cum += sh.rtmass[d];
+    }
+    above += cum;
+    const uint32_t digit = 255u - (uint32_t)sel;
+    prefix |= digit << shift;
+    pmask |= 255u << shift;
+    if (pass == 3) {
+      out.at_count = sh.rtcnt[sel];
+      out.at_weight = sh.rtmass[sel];
+    }
+    __syncthreads();
+  }
+  out.tau = prefix;
+  out.above = above;
+  out.target = target;
+  return out;
+}
+
 // The id (global) of the nth (1-based) element, in ascending id order over
 // the cluster, for which pred(local index) holds.  Same result in all CTAs.
 template <class Pred>
 SPEC_DEV int nth_in_cluster(const Slice& sl, int nth, Pred pred, int rank, int CS, int& ph,
                             Shared& sh) {
   const int seg = (sl.n + kST - 1) / kST;
-  const int s0 = min(threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
+  const int s0 = min((int)threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
   int c = 0;
   for (int k = s0; k < s1; ++k) c += pred(k) ? 1 : 0;
   int tot;
   const int excl = block_excl_scan_i(c, &tot, sh);
-  // rank prefix
-  Slot* s = &sh.slots[ph & 3];
-  if (threadIdx.x == 0) s->a = (unsigned long long)tot;
-  cluster_sync();
+  cluster_allgather(Slot{(unsigned long long)tot, 0ull}, CS, ph, sh);
   int before = 0, owner = -1;
   for (int r = 0; r < CS; ++r) {
-    const int tr = (int)dsmem_ld_u64(&s->a, r);
+    const int tr = (int)sh.gath[r].a;
     if (owner < 0 && before + tr >= nth) owner = r;
     if (owner < 0) before += tr;
   }
-  ++ph;
   int found = INT_MAX;
   if (owner == rank) {
     const int local = nth - before;
@@ -334,162 +736,81 @@ SPEC_DEV int nth_in_cluster(const Slice& sl, int nth, Pred pred, int rank, int C
     }
   }
   found = block_min_i(found, sh);
-  Slot mine{(unsigned long long)(unsigned)found, 0ull};
-  const Slot o = cluster_from(mine, owner < 0 ? 0 : owner, ph, sh);
+  const Slot o = cluster_from(Slot{(unsigned long long)(unsigned)found, 0ull},
+                              owner < 0 ? 0 : owner, CS, ph, sh);
   return owner < 0 ? INT_MAX : (int)(unsigned)o.a;
 }
 
-// Radix selection, most significant digit first, of the position in
-// (key desc, id asc) order where the running weight reaches `target`.
-// Weight = 1 per element (by_mass = false) or its 2^-40 fixed-point mass.
-// Elements considered: those with keep(k).  Returns tau (exact key), the
-// weight strictly above tau, and the count/weight at tau.
-struct Sel {
-  uint32_t tau;
-  unsigned long long above;
-  unsigned long long at_weight;
-  unsigned long long total;
-  uint32_t at_count;
-};
-
-template <class Keep, class Weight>
-SPEC_DEV Sel radix_select(const Slice& sl, bool target_is_fraction, double frac,
-                          unsigned long long target_abs, Keep keep, Weight weight, int CS, int& ph,
-                          Shared& sh) {
-  const int lane = threadIdx.x & 31;
-  uint32_t prefix = 0, pmask = 0;
-  unsigned long long above = 0, target = target_abs, total = 0;
-  Sel out{};
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const int h = pass & 1;
-    for (int i = threadIdx.x; i < 256; i += kST) {
-      sh.hmass[h][i] = 0ull;
-      sh.hcnt[h][i] = 0u;
+SPEC_DEV Trunc truncate_radix(const SP& p, const Slice& sl, float m, int rank, int CS, int& ph,
+                              Shared& sh) {
+  Trunc tr{0u, INT_MAX, DF{0.f, 0.f}, true};
+  cluster_sync();  // other CTAs may still read this CTA's coarse histogram
+  if (p.top_k > 0 && p.top_k < p.V) {
+    const Sel s = radix_select(
+        sl, false, 0.0, (unsigned long long)p.top_k, [](int, uint32_t) { return true; },
+        [](int) { return 1ull; }, CS, ph, sh);
+    const int need = (int)(s.target - s.above);
+    tr.tau = s.tau;
+    if ((uint32_t)need >= s.at_count) {
+      tr.tie = INT_MAX;
+    } else {
+      const uint32_t tau = s.tau;
+      tr.tie = nth_in_cluster(
+          sl, need, [&](int k) { return okey(sl.buf[k]) == tau; }, rank, CS, ph, sh);
     }
-    __syncthreads();
-    const int iters = (sl.n + kST - 1) / kST;
-    for (int it = 0; it < iters; ++it) {
-      const int k = threadIdx.x + it * kST;
-      bool act = false;
-      uint32_t key = 0;
-      unsigned long long wgt = 0;
-      if (k < sl.n) {
-        key = okey(sl.buf[k]);
-        act = ((key & pmask) == prefix) && keep(k, key);
-        if (act) wgt = weight(k);
-      }
-      const uint32_t digit = (key >> shift) & 255u;
-      const unsigned peers = __match_any_sync(kFull, act ? digit : 256u + lane);
-      // fixed-point weight <= 2^41: split so 32-lane sums fit in 32 bits
-      const unsigned hi = __reduce_add_sync(peers, (unsigned)(wgt >> 20));
-      const unsigned lo = __reduce_add_sync(peers, (unsigned)(wgt & 0xFFFFFull));
-      if (act && lane == __ffs(peers) - 1) {
-        atomicAdd(&sh.hcnt[h][digit], (unsigned)__popc(peers));
-        atomicAdd(&sh.hmass[h][digit], ((unsigned long long)hi << 20) + lo);
-      }
-    }
-    __syncthreads();
-    cluster_sync();
-    for (int d = threadIdx.x; d < 256; d += kST) {
-      unsigned long long m = 0;
-      uint32_t c = 0;
-      for (int r = 0; r < CS; ++r) {
-        m += dsmem_ld_u64(&sh.hmass[h][d], r);
-        c += dsmem_ld_u32(&sh.hcnt[h][d], r);
-      }
-      sh.tot_mass[d] = m;
-      sh.tot_cnt[d] = c;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane L holds digits 255-8L .. 248-8L (descending)
-      unsigned long long ls = 0;
-      for (int j = 0; j < 8; ++j) ls += sh.tot_mass[255 - 8 * lane - j];
-      if (pass == 0) {
-        unsigned long long t = ls;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
-        total = t;
-        if (target_is_fraction) {
-          const double thr = ceil(frac * (double)t);
-          target = thr < 1.0 ? 1ull : (unsigned long long)thr;
-          if (target > t) target = t;
-        }
-      }
-      unsigned long long incl = ls;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const unsigned long long need = target - above;
-      const unsigned hit = __ballot_sync(kFull, incl >= need);
-      const int L = hit ? __ffs(hit) - 1 : 31;
-      if (lane == L) {
-        unsigned long long cum = incl - ls;
-        int dsel = 248 - 8 * L;
-        for (int j = 0; j < 8; ++j) {
-          const int d = 255 - 8 * L - j;
-          if (cum + sh.tot_mass[d] >= need) {
-            dsel = d;
-            break;
-          }
-          cum += sh.tot_mass[d];
-        }
-        sh.bu[0] = (uint32_t)dsel;
-        sh.bull[0] = cum;  // weight in digits above dsel (within the prefix)
-      }
-      if (lane == 0) sh.bull[1] = total;
-    }
-    __syncthreads();
-    const uint32_t dsel = sh.bu[0];
-    above += sh.bull[0];
-    total = sh.bull[1];
-    if (pass == 0 && target_is_fraction) {
-      const double thr = ceil(frac * (double)total);
-      target = thr < 1.0 ? 1ull : (unsigned long long)thr;
-      if (target > total) target = total;
-    }
-    prefix |= dsel << shift;
-    pmask |= 255u << shift;
-    if (pass == 3) {
-      out.at_count = sh.tot_cnt[dsel];
-      out.at_weight = sh.tot_mass[dsel];
-    }
-    __syncthreads();
   }
-  out.tau = prefix;
-  out.above = above;
-  out.total = total;
-  // stash the target for the caller (needed for the tie count)
-  sh.bull[0] = target;
-  __syncthreads();
-  return out;
+  if (p.top_p > 0.f && p.top_p < 1.f) {
+    const uint32_t tk = tr.tau;
+    const int tc = tr.tie;
+    const float T = p.T, invT = p.invT;
+    auto keep_k = [&](int k, uint32_t key) { return is_kept(key, sl.lo + k, tk, tc); };
+    auto mass = [&](int k) {
+      const float e = texp(sl.buf[k], m, T, invT);
+      return (unsigned long long)__float2ull_rn(e * 1099511627776.0f);  // 2^40
+    };
+    const Sel s = radix_select(sl, true, (double)p.top_p, 0ull, keep_k, mass, CS, ph, sh);
+    const unsigned long long e_tau = s.at_count ? s.at_weight / s.at_count : 0ull;
+    unsigned long long need = 1;
+    if (e_tau > 0 && s.target > s.above) need = (s.target - s.above + e_tau - 1) / e_tau;
+    if (need < 1) need = 1;
+    if (need > s.at_count) need = s.at_count;
+    const uint32_t tau = s.tau;
+    int tie;
+    if (need == s.at_count) {
+      tie = (tau == tk) ? tc : INT_MAX;
+    } else {
+      tie = nth_in_cluster(
+          sl, (int)need,
+          [&](int k) {
+            const uint32_t key = okey(sl.buf[k]);
+            return key == tau && is_kept(key, sl.lo + k, tk, tc);
+          },
+          rank, CS, ph, sh);
+    }
+    tr.tau = tau;
+    tr.tie = tie;
+  }
+  return tr;
 }
 
-// Draw: the first id whose running sum (ascending id order over the
-// cluster) of the slice values exceeds u * total.  Returns -2 if the total
-// is zero.  Same result in all CTAs.
+// ---------------------------------------------------------------- the draw
+// The first id whose running sum (ascending id order over the cluster) of
+// the slice values exceeds u * total; -2 if the total is zero.  Same result
+// in all CTAs.
 SPEC_DEV int draw_from_slice(const Slice& sl, float u, int rank, int CS, int& ph, Shared& sh) {
   const int seg = (sl.n + kST - 1) / kST;
-  const int s0 = min(threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
+  const int s0 = min((int)threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
   float run = 0.f;
   for (int k = s0; k < s1; ++k) run += sl.buf[k];
   float tot;
   const float excl = block_excl_scan_f(run, &tot, sh);
-  Slot* s = &sh.slots[ph & 3];
-  if (threadIdx.x == 0) s->a = (unsigned long long)__float_as_uint(tot);
-  cluster_sync();
-  float prefix = 0.f, my_prefix = 0.f;
-  float tots[kMaxCS];
-  for (int r = 0; r < CS; ++r) {
-    tots[r] = __uint_as_float((uint32_t)dsmem_ld_u64(&s->a, r));
-  }
-  ++ph;
-  float pre[kMaxCS + 1];
+  cluster_allgather(Slot{(unsigned long long)__float_as_uint(tot), 0ull}, CS, ph, sh);
+  float pre[kMaxCS + 1], tots[kMaxCS];
   pre[0] = 0.f;
-  for (int r = 0; r < CS; ++r) pre[r + 1] = pre[r] + tots[r];
+  for (int r = 0; r < CS; ++r) {
+    tots[r] = __uint_as_float((uint32_t)sh.gath[r].a);
+    pre[r + 1] = pre[r] + tots[r];
+  }
   const float W = pre[CS];
   if (!(W > 0.f)) return -2;
   const float target = u * W;
@@ -499,8 +820,7 @@ SPEC_DEV int draw_from_slice(const Slice& sl, float u, int rank, int CS, int& ph
   if (owner < 0)
     for (int r = CS - 1; r >= 0; --r)
       if (owner < 0 && tots[r] > 0.f) owner = r;
-  prefix = pre[owner];
-  (void)my_prefix;
+  const float prefix = pre[owner];
   int found = INT_MAX;
   if (owner == rank) {
     if (prefix + (excl + run) > target || threadIdx.x == kST - 1) {
@@ -513,58 +833,80 @@ SPEC_DEV int draw_from_slice(const Slice& sl, float u, int rank, int CS, int& ph
         }
       }
     }
+    found = block_min_i(found, sh);
+    if (found == INT_MAX) {
+      // rounding left nothing above target: take the last nonzero entry
+      int last = -1;
+      for (int k = s0; k < s1; ++k)
+        if (sl.buf[k] > 0.f) last = k;
+      const int neg = block_min_i(-last, sh);  // -(largest index)
+      found = (neg <= 0) ? -neg : INT_MAX;
+    }
   }
-  found = block_min_i(found, sh);
-  if (owner == rank && found == INT_MAX) {
-    // rounding left nothing above target: take the last nonzero entry
-    int last = -1;
-    for (int k = s0; k < s1; ++k)
-      if (sl.buf[k] > 0.f) last = k;
-    const int neg = block_min_i(-last, sh);  // -(largest index)
-    found = (neg <= 0) ? -neg : INT_MAX;
-  }
-  Slot mine{(unsigned long long)(unsigned)(found == INT_MAX ? 0 : sl.lo + found), 0ull};
-  const Slot o = cluster_from(mine, owner, ph, sh);
+  const Slot o = cluster_from(
+      Slot{(unsigned long long)(unsigned)(found == INT_MAX ? 0 : sl.lo + found), 0ull}, owner, CS,
+      ph, sh);
   return (int)(unsigned)o.a;
 }
 
-SPEC_DEV RowStat load_stat(const RowStat* s) {
-  RowStat r;
-  const int4* src = reinterpret_cast<const int4*>(s);
-  const int4 a = __ldcg(src), b2 = __ldcg(src + 1);
-  memcpy(&r, &a, 16);
-  memcpy(reinterpret_cast<char*>(&r) + 16, &b2, 16);
-  return r;
-}
-
-// p_row(x) from the row's statistics and one logit
-SPEC_DEV float p_of(const SP& p, const RowStat& st, float l, int id) {
-  if (!is_kept(okey(l), id, st.tau, st.tie_cut)) return 0.f;
-  return texp(l, st.m, p.T, p.invT) / st.Z;
-}
-
-// Fill the slice with p of row `row` (logits already loaded in the slice).
-SPEC_DEV void slice_to_p(const SP& p, const RowStat& st, Slice& sl) {
-  for (int k = threadIdx.x; k < sl.n; k += kST) sl.buf[k] = p_of(p, st, sl.buf[k], sl.lo + k);
-  __syncthreads();
-}
-
 // ---------------------------------------------------------------- the kernel
+// One cluster per target row.  Every row computes its own outcome:
+//   chain row i < R-1: is draft i+1 accepted? if not, the correction drawn
+//     from norm(max(0, p_i - q_i));  chain row R-1: the bonus drawn from p;
+//   tree node v: the first accepted child (residual p' updated after each
+//     rejected child) or, if none, the final token drawn from p'.
+// The cluster that finishes a sequence's last row assembles the sequence.
 __global__ void __launch_bounds__(kST, 1) sampler_kernel(const SP p) {
-  extern __shared__ __align__(16) float sbuf[];
+  extern __shared__ __align__(16) uint8_t dyn[];
+  float* Lb = reinterpret_cast<float*>(dyn);
+  float* Eb = Lb + p.slice;
+  Scratch sc;
+  sc.cand = reinterpret_cast<uint64_t*>(Eb + p.slice);
+  sc.gk = sc.cand + kCandMax;
+  sc.sk = sc.gk + kCandMax;
+  sc.candE = reinterpret_cast<float*>(sc.sk + kCandMax);
+  sc.ge = sc.candE + kCandMax;
+  sc.se = sc.ge + kCandMax;
   __shared__ Shared sh;
   const int rank = (int)cluster_ctarank();
   const int CS = (int)cluster_nctarank();
   const int row = blockIdx.y;
-  const int b = row / p.R;
-  const int i = row % p.R;
-  Slice sl{sbuf, rank * p.slice, 0};
+  const int R = p.R;
+  const int b = row / R;
+  const int i = row % R;
+  Slice sl{Lb, rank * p.slice, 0};
   sl.n = max(0, min(p.slice, p.V - sl.lo));
+  Slice sw{Eb, sl.lo, sl.n};
   int ph = 0;
   uint32_t bar_phase = 0;
+
+  // the q row this row may need for its residual: warm it into L2 now
+  const float* qrow = nullptr;
+  if (!p.greedy && p.q) {
+    if (p.tree)
+      qrow = p.q + ((size_t)b * R + i) * p.V;
+    else if (i < R - 1)
+      qrow = p.q + ((size_t)b * (R - 1) + i) * p.V;
+  }
   if (threadIdx.x == 0) {
     mbar_init(&sh.bar, 1);
     fence_mbar_init();
+    if (qrow && p.qbulk && sl.n > 0) prefetch_l2(qrow + sl.lo, (uint32_t)sl.n * 4u);
+  }
+  if (p.tree)
+    for (int c = threadIdx.x; c < R; c += kST) {
+      sh.par[c] = p.parent[(size_t)b * R + c];
+      sh.tok[c] = p.tokens[(size_t)b * R + c];
+    }
+  // scalars of this row's test, loaded early
+  float u_test = 0.f, u_final = 0.f;
+  int x_draft = -1;
+  if (!p.greedy) {
+    u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    if (!p.tree && i < R - 1) {
+      u_test = __ldg(&p.u[(size_t)b * R + i]);
+      x_draft = __ldg(&p.tokens[(size_t)b * (R - 1) + i]);
+    }
   }
   __syncthreads();
 
@@ -585,336 +927,218 @@ __global__ void __launch_bounds__(kST, 1) sampler_kernel(const SP p) {
   }
   bad = block_or(bad, sh);
   block_max_arg(mv, mi, sh);
-  {
-    Slot* s = &sh.slots[ph & 3];
-    if (threadIdx.x == 0) {
-      s->a = ((unsigned long long)__float_as_uint(mv) << 32) | (unsigned)mi;
-      s->b = (unsigned long long)bad;
+  cluster_allgather(Slot{((unsigned long long)__float_as_uint(mv) << 32) | (unsigned)mi,
+                         (unsigned long long)bad},
+                    CS, ph, sh);
+  for (int r = 0; r < CS; ++r) {
+    const unsigned long long a = sh.gath[r].a;
+    const float ov = __uint_as_float((uint32_t)(a >> 32));
+    const int oi = (int)(uint32_t)a;
+    bad |= (int)sh.gath[r].b;
+    if (ov > mv || (ov == mv && oi < mi)) {
+      mv = ov;
+      mi = oi;
     }
-    cluster_sync();
-    for (int r = 0; r < CS; ++r) {
-      const unsigned long long a = dsmem_ld_u64(&s->a, r);
-      const float ov = __uint_as_float((uint32_t)(a >> 32));
-      const int oi = (int)(uint32_t)a;
-      bad |= (int)dsmem_ld_u64(&s->b, r);
-      if (ov > mv || (ov == mv && oi < mi)) {
-        mv = ov;
-        mi = oi;
-      }
-    }
-    ++ph;
   }
   if (mv == -INFINITY) bad = 1;  // every token banned: no distribution
   const float m = mv;
-  RowStat st{};
-  st.m = m;
-  st.argmax = mi;
-  st.flags = bad;
-  st.tau = 0u;
-  st.tie_cut = INT_MAX;
-  st.Z = 1.f;
+  Outcome oc{0, -1, 0, bad};
 
-  if (!p.greedy && !bad) {
-    // ---- 3. truncation (top-k by count, then top-p by mass)
-    if (p.top_k > 0 && p.top_k < p.V) {
-      const Sel s = radix_select(
-          sl, false, 0.0, (unsigned long long)p.top_k, [](int, uint32_t) { return true; },
-          [](int) { return 1ull; }, CS, ph, sh);
-      const unsigned long long target = sh.bull[0];
-      const int need = (int)(target - s.above);  // ties at tau to keep (>= 1)
-      st.tau = s.tau;
-      if ((uint32_t)need >= s.at_count) {
-        st.tie_cut = INT_MAX;
+  if (p.greedy) {
+    // ---- greedy: the argmax decides everything
+    if (!bad) {
+      if (!p.tree) {
+        if (i < R - 1) oc.accept = (__ldg(&p.tokens[(size_t)b * (R - 1) + i]) == mi) ? 1 : 0;
+        oc.token = mi;
       } else {
-        const uint32_t tau = s.tau;
-        st.tie_cut = nth_in_cluster(
-            sl, need, [&](int k) { return okey(sl.buf[k]) == tau; }, rank, CS, ph, sh);
+        oc.accept = -1;
+        for (int c = i + 1; c < R; ++c)
+          if (sh.par[c] == i && sh.tok[c] == mi) {
+            oc.accept = c;
+            break;
+          }
+        oc.token = mi;
       }
     }
-    if (p.top_p > 0.f && p.top_p < 1.f) {
-      const uint32_t tk = st.tau;
-      const int tc = st.tie_cut;
-      const float T = p.T, invT = p.invT;
-      auto keep_k = [&](int k, uint32_t key) { return is_kept(key, sl.lo + k, tk, tc); };
-      auto mass = [&](int k) {
-        const float e = texp(sl.buf[k], m, T, invT);
-        return (unsigned long long)__float2ull_rn(e * 1099511627776.0f);  // 2^40
-      };
-      const Sel s = radix_select(sl, true, (double)p.top_p, 0ull, keep_k, mass, CS, ph, sh);
-      const unsigned long long target = sh.bull[0];
-      const unsigned long long e_tau = s.at_count ? s.at_weight / s.at_count : 0ull;
-      unsigned long long need = 1;
-      if (e_tau > 0 && target > s.above) need = (target - s.above + e_tau - 1) / e_tau;
-      if (need < 1) need = 1;
-      if (need > s.at_count) need = s.at_count;
-      const uint32_t tau = s.tau;
-      int tie;
-      if (need == s.at_count) {
-        tie = (tau == tk) ? tc : INT_MAX;
-      } else {
-        tie = nth_in_cluster(
-            sl, (int)need,
-            [&](int k) {
-              const uint32_t key = okey(sl.buf[k]);
-              return key == tau && is_kept(key, sl.lo + k, tk, tc);
-            },
-            rank, CS, ph, sh);
-      }
-      st.tau = tau;
-      st.tie_cut = tie;
-    }
-    // ---- 4. normaliser over the kept set (compensated per thread, fp64 tree)
-    float sum = 0.f, cmp = 0.f;
+  } else if (!bad) {
+    // ---- 3. exp values, normaliser, truncation
+    Kahan acc;
     for (int k = threadIdx.x; k < sl.n; k += kST) {
-      const float x = sl.buf[k];
-      if (!is_kept(okey(x), sl.lo + k, st.tau, st.tie_cut)) continue;
-      const float y = texp(x, m, p.T, p.invT) - cmp;
-      const float t = sum + y;
-      cmp = (t - sum) - y;
-      sum = t;
+      const float e = texp(sl.buf[k], m, p.T, p.invT);
+      Eb[k] = e;
+      acc.add(e);
     }
-    double z = block_sum_d((double)sum - (double)cmp, sh);
-    z = cluster_sum_d(z, CS, ph, sh);
-    st.Z = (float)z;
+    const DF zall = cluster_sum_df(block_sum_df(acc.df(), sh), CS, ph, sh);
+    Trunc tr{0u, INT_MAX, zall, true};
+    if ((p.top_k > 0 && p.top_k < p.V) || (p.top_p > 0.f && p.top_p < 1.f)) {
+      tr = truncate_fast(p, sl, Eb, sc, m, zall, rank, CS, ph, sh);
+      if (!tr.ok) {
+        tr = truncate_radix(p, sl, m, rank, CS, ph, sh);
+        const uint32_t tau = tr.tau;
+        const int tie = tr.tie;
+        tr.Z = cluster_masked_sum(
+            sl, Eb, [&](int k) { return is_kept(okey(sl.buf[k]), sl.lo + k, tau, tie); }, CS,
+            ph, sh);
+      }
+    }
+    const float invZ = 1.0f / (float)df_d(tr.Z);
+    const bool truncated = tr.tau != 0u || tr.tie != INT_MAX;
+    // p in place of the exp values (0 outside the kept set)
+    if (truncated) {
+      for (int k = threadIdx.x; k < sl.n; k += kST)
+        Eb[k] = is_kept(okey(sl.buf[k]), sl.lo + k, tr.tau, tr.tie) ? Eb[k] * invZ : 0.f;
+    } else {
+      for (int k = threadIdx.x; k < sl.n; k += kST) Eb[k] *= invZ;
+    }
+    __syncthreads();
     if (p.p_out) {
       float* dst = p.p_out + (size_t)row * p.V + sl.lo;
-      for (int k = threadIdx.x; k < sl.n; k += kST) dst[k] = p_of(p, st, sl.buf[k], sl.lo + k);
+      for (int k = threadIdx.x; k < sl.n; k += kST) dst[k] = Eb[k];
     }
-  }
 
-  // ---- 5. publish the row statistics; the last row of a sequence continues
-  if (rank == 0 && threadIdx.x == 0) {
-    p.stats[row] = st;
-    __threadfence();
-    const int old = atomicAdd(&p.seq_count[b], 1);
-    sh.bi[0] = (old == p.R - 1) ? 1 : 0;
-  }
-  cluster_sync();
-  const int last = (int)dsmem_ld_u32(&sh.bi[0], 0);
-  cluster_sync();
-  if (!last) return;
-  __threadfence();
-
-  const int R = p.R;
-  int32_t* emitted = p.emitted + (size_t)b * R;
-  int status = 0;
-  int k_emit = 0;
-
-  // ---- 6a. greedy walks (thread 0 of rank 0 writes the outputs)
-  if (p.greedy) {
-    if (rank == 0 && threadIdx.x == 0) {
-      int nonfin = 0;
-      for (int r = 0; r < R; ++r) nonfin |= load_stat(&p.stats[(size_t)b * R + r]).flags;
-      int acc = 0;
-      if (nonfin) {
-        status |= SPEC_SEQ_NONFINITE;
-        acc = -1;
-      } else if (!p.tree) {
-        for (int r = 0; r < R; ++r) {
-          const int a = load_stat(&p.stats[(size_t)b * R + r]).argmax;
-          if (r == R - 1) {
-            emitted[k_emit++] = a;
-            break;
-          }
-          const int x = p.tokens[(size_t)b * (R - 1) + r];
-          if (x == a) {
-            emitted[k_emit++] = x;
-            ++acc;
-            if (x == p.eos) break;
-          } else {
-            emitted[k_emit++] = a;
-            break;
-          }
-        }
-      } else {
-        int v = 0;
-        while (true) {
-          const int a = load_stat(&p.stats[(size_t)b * R + v]).argmax;
-          int nxt = -1;
-          for (int c = v + 1; c < R; ++c)
-            if (p.parent[(size_t)b * R + c] == v && p.tokens[(size_t)b * R + c] == a) {
-              nxt = c;
-              break;
-            }
-          emitted[k_emit++] = a;
-          if (nxt >= 0) p.path[(size_t)b * R + acc++] = nxt;
-          if (nxt < 0 || a == p.eos) break;
-          v = nxt;
-        }
-        for (int c = acc; c < R; ++c) p.path[(size_t)b * R + c] = -1;
+    if (!p.tree) {
+      // ---- 4a. chain: this row's test, then its correction or bonus draw
+      bool draw = true;
+      bool resid = false;
+      if (i < R - 1) {
+        const int x = x_draft;
+        const bool xin = x >= 0 && x < p.V;
+        const float qx = xin ? __ldg(&qrow[x]) : 0.f;
+        cluster_sync();  // p complete in every CTA
+        const float px =
+            xin ? dsmem_ld_f32(&Eb[x - (x / p.slice) * p.slice], (uint32_t)(x / p.slice)) : 0.f;
+        if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
+        oc.accept = (u_test * qx < px) ? 1 : 0;
+        cluster_sync();  // nobody rewrites p before every CTA has read p(x)
+        draw = !oc.accept;
+        resid = true;
       }
-      for (int c = (nonfin ? 0 : k_emit); c < R; ++c) emitted[c] = -1;
-      if (nonfin && p.tree)
-        for (int c = 0; c < R; ++c) p.path[(size_t)b * R + c] = -1;
-      p.acc_len[b] = acc;
-      if (p.status) p.status[b] = status;
-      p.seq_count[b] = 0;
-    }
-    return;
-  }
-
-  // ---- 6b. sampling: read statistics of every row of this sequence
-  int nonfin = 0;
-  for (int r = 0; r < R; ++r) nonfin |= load_stat(&p.stats[(size_t)b * R + r]).flags;
-  if (nonfin) {
-    if (rank == 0 && threadIdx.x == 0) {
-      for (int c = 0; c < R; ++c) emitted[c] = -1;
-      if (p.tree)
-        for (int c = 0; c < R; ++c) p.path[(size_t)b * R + c] = -1;
-      p.acc_len[b] = -1;
-      if (p.status) p.status[b] = SPEC_SEQ_NONFINITE;
-      p.seq_count[b] = 0;
-    }
-    return;
-  }
-
-  const float u_final = p.u[(size_t)b * R + (R - 1)];
-  if (!p.tree) {
-    // chain walk: thread 0 of every CTA computes the same decisions
-    int acc = 0, draw_row = -1, resid = 0, stop = 0;
-    for (int r = 0; r < R - 1; ++r) {
-      const int x = p.tokens[(size_t)b * (R - 1) + r];
-      float px = 0.f, qx = 0.f;
-      if (x >= 0 && x < p.V) {
-        const RowStat srow = load_stat(&p.stats[(size_t)b * R + r]);
-        px = p_of(p, srow, __ldcg(&p.logits[((size_t)b * R + r) * p.V + x]), x);
-        qx = __ldcg(&p.q[((size_t)b * (R - 1) + r) * p.V + x]);
+      if (draw) {
+        if (resid) {
+          for (int k = threadIdx.x; k < sl.n; k += kST)
+            Eb[k] = fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f);
+          __syncthreads();
+        }
+        int tok = draw_from_slice(sw, u_final, rank, CS, ph, sh);
+        if (tok == -2) {  // residual with zero mass (rounding only): draw from p
+          oc.status |= SPEC_SEQ_RESID_ZERO;
+          for (int k = threadIdx.x; k < sl.n; k += kST)
+            Eb[k] = is_kept(okey(sl.buf[k]), sl.lo + k, tr.tau, tr.tie)
+                        ? texp(sl.buf[k], m, p.T, p.invT) * invZ
+                        : 0.f;
+          __syncthreads();
+          tok = draw_from_slice(sw, u_final, rank, CS, ph, sh);
+        }
+        oc.token = tok;
       }
-      if (qx == 0.f) status |= SPEC_SEQ_QZERO;
-      if (p.u[(size_t)b * R + r] * qx < px) {
-        ++acc;
-        if (x == p.eos) {
-          stop = 1;
+    } else {
+      // ---- 4b. tree node: children in storage order against the running p'
+      oc.accept = -1;
+      for (int c = i + 1; c < R; ++c) {
+        if (sh.par[c] != i) continue;
+        const int t = sh.tok[c];
+        const bool tin = t >= 0 && t < p.V;
+        const float qx = tin ? __ldg(&qrow[t]) : 0.f;
+        cluster_sync();  // p' complete everywhere
+        const float pt =
+            tin ? dsmem_ld_f32(&Eb[t - (t / p.slice) * p.slice], (uint32_t)(t / p.slice)) : 0.f;
+        cluster_sync();  // nobody rewrites p' before every CTA has read it
+        if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
+        if (__ldg(&p.u[(size_t)b * R + (c - 1)]) * qx < pt) {
+          oc.accept = c;
           break;
         }
-      } else {
-        draw_row = r;
-        resid = 1;
-        break;
-      }
-    }
-    if (!stop && draw_row < 0) draw_row = R - 1;
-    int tok = -1;
-    if (!stop) {
-      const RowStat sr = load_stat(&p.stats[(size_t)b * R + draw_row]);
-      load_row(p, p.logits + ((size_t)b * R + draw_row) * p.V, sl, sh, bar_phase);
-      const float* qrow = p.q + ((size_t)b * (R - 1) + (resid ? draw_row : 0)) * p.V + sl.lo;
-      for (int k = threadIdx.x; k < sl.n; k += kST) {
-        const float pv = p_of(p, sr, sl.buf[k], sl.lo + k);
-        sl.buf[k] = resid ? fmaxf(pv - __ldcg(&qrow[k]), 0.f) : pv;
-      }
-      __syncthreads();
-      tok = draw_from_slice(sl, u_final, rank, CS, ph, sh);
-      if (tok == -2) {
-        // residual with zero mass (rounding only): draw from p instead
-        status |= SPEC_SEQ_RESID_ZERO;
-        load_row(p, p.logits + ((size_t)b * R + draw_row) * p.V, sl, sh, bar_phase);
-        slice_to_p(p, sr, sl);
-        tok = draw_from_slice(sl, u_final, rank, CS, ph, sh);
-      }
-    }
-    if (rank == 0 && threadIdx.x == 0) {
-      for (int r = 0; r < acc; ++r) emitted[r] = p.tokens[(size_t)b * (R - 1) + r];
-      int kk = acc;
-      if (!stop) emitted[kk++] = tok;
-      for (int c = kk; c < R; ++c) emitted[c] = -1;
-      p.acc_len[b] = acc;
-      if (p.status) p.status[b] = status;
-      p.seq_count[b] = 0;
-    }
-    cluster_sync();  // keep every CTA's shared memory alive until all reads finish
-    return;
-  }
-
-  // ---- 6c. tree walk with a dense running residual p' in the slices
-  const int N = R;
-  for (int c = threadIdx.x; c < N; c += kST) {
-    sh.par[c] = p.parent[(size_t)b * N + c];
-    sh.tok[c] = p.tokens[(size_t)b * N + c];
-  }
-  __syncthreads();
-  int v = 0, acc = 0, done = 0;
-  int32_t* path = p.path + (size_t)b * N;
-  {
-    const RowStat s0 = load_stat(&p.stats[(size_t)b * N]);
-    load_row(p, p.logits + (size_t)b * N * p.V, sl, sh, bar_phase);
-    slice_to_p(p, s0, sl);
-  }
-  while (!done) {
-    int moved = 0;
-    for (int c = v + 1; c < N && !moved; ++c) {
-      if (sh.par[c] != v) continue;
-      const int t = sh.tok[c];
-      cluster_sync();  // p' complete everywhere
-      float pt = 0.f;
-      if (t >= 0 && t < p.V) {
-        const int owner = t / p.slice;
-        pt = dsmem_ld_f32(&sl.buf[t - owner * p.slice], (uint32_t)owner);
-      }
-      cluster_sync();  // nobody rewrites p' before every CTA has read it
-      const float qx = (t >= 0 && t < p.V) ? __ldcg(&p.q[((size_t)b * N + v) * p.V + t]) : 0.f;
-      if (qx == 0.f) status |= SPEC_SEQ_QZERO;
-      if (p.u[(size_t)b * N + (c - 1)] * qx < pt) {
-        if (rank == 0 && threadIdx.x == 0) {
-          emitted[acc] = t;
-          path[acc] = c;
-        }
-        ++acc;
-        v = c;
-        moved = 1;
-        if (t == p.eos) {
-          done = 1;
-        } else {
-          const RowStat sv = load_stat(&p.stats[(size_t)b * N + v]);
-          load_row(p, p.logits + ((size_t)b * N + v) * p.V, sl, sh, bar_phase);
-          slice_to_p(p, sv, sl);
-        }
-      } else {
         // p' <- norm(max(0, p' - q_v))
-        const float* qrow = p.q + ((size_t)b * N + v) * p.V + sl.lo;
-        float sum = 0.f, cmp = 0.f;
-        for (int k = threadIdx.x; k < sl.n; k += kST) {
-          const float y = fmaxf(sl.buf[k] - __ldcg(&qrow[k]), 0.f) - cmp;
-          const float tt = sum + y;
-          cmp = (tt - sum) - y;
-          sum = tt;
-        }
-        double W = block_sum_d((double)sum - (double)cmp, sh);
-        W = cluster_sum_d(W, CS, ph, sh);
-        if (W > 0.0) {
-          const float Wf = (float)W;
+        Kahan w;
+        for (int k = threadIdx.x; k < sl.n; k += kST)
+          w.add(fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f));
+        const DF W = cluster_sum_df(block_sum_df(w.df(), sh), CS, ph, sh);
+        const float Wf = (float)df_d(W);
+        if (Wf > 0.f) {
+          const float invW = 1.0f / Wf;
           for (int k = threadIdx.x; k < sl.n; k += kST)
-            sl.buf[k] = fmaxf(sl.buf[k] - __ldcg(&qrow[k]), 0.f) / Wf;
+            Eb[k] = fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f) * invW;
         } else {
-          status |= SPEC_SEQ_RESID_ZERO;
+          oc.status |= SPEC_SEQ_RESID_ZERO;
         }
         __syncthreads();
       }
+      if (oc.accept < 0) oc.token = draw_from_slice(sw, u_final, rank, CS, ph, sh);
     }
-    if (!moved && !done) {
-      const int tok = draw_from_slice(sl, u_final, rank, CS, ph, sh);
-      if (rank == 0 && threadIdx.x == 0) emitted[acc] = tok;
-      done = 1;
-      if (rank == 0 && threadIdx.x == 0) {
-        for (int c = acc + 1; c < N; ++c) emitted[c] = -1;
+  }
+
+  // ---- 5. publish the outcome; the last row of the sequence assembles it
+  cluster_sync();  // every CTA is done with the others' shared memory
+  if (rank != 0 || threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int last = 0;
+  if (lane == 0) {
+    p.outcomes[row] = oc;
+    __threadfence();
+    last = atomicAdd(&p.seq_count[b], 1) == R - 1;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence();
+  // warp 0 loads the sequence's outcomes (and its draft tokens) in parallel
+  for (int r = lane; r < R; r += 32) {
+    const int4 v = __ldcg(reinterpret_cast<const int4*>(&p.outcomes[(size_t)b * R + r]));
+    sh.outs[r] = Outcome{v.x, v.y, v.z, v.w};
+    sh.tok[r] = p.tree ? __ldg(&p.tokens[(size_t)b * R + r])
+                       : (r < R - 1 ? __ldg(&p.tokens[(size_t)b * (R - 1) + r]) : -1);
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  int32_t* emitted = p.emitted + (size_t)b * R;
+  int nonfin = 0, status = 0, acc = 0, k = 0;
+  for (int r = 0; r < R; ++r) nonfin |= sh.outs[r].flags;
+  if (nonfin) {
+    acc = -1;
+    status = SPEC_SEQ_NONFINITE;
+  } else if (!p.tree) {
+    for (int r = 0; r < R; ++r) {
+      const Outcome& o = sh.outs[r];
+      status |= o.status;
+      if (r < R - 1 && o.accept) {
+        const int x = sh.tok[r];
+        emitted[k++] = x;
+        ++acc;
+        if (x == p.eos) break;
+        continue;
       }
-    } else if (done && rank == 0 && threadIdx.x == 0) {
-      for (int c = acc; c < N; ++c) emitted[c] = -1;
+      emitted[k++] = o.token;
+      break;
+    }
+  } else {
+    int32_t* path = p.path + (size_t)b * R;
+    int v = 0;
+    while (true) {
+      const Outcome& o = sh.outs[v];
+      status |= o.status;
+      if (o.accept > v) {
+        const int t = sh.tok[o.accept];
+        emitted[k++] = t;
+        path[acc++] = o.accept;
+        v = o.accept;
+        if (t == p.eos) break;
+        continue;
+      }
+      emitted[k++] = o.token;
+      break;
     }
   }
-  if (rank == 0 && threadIdx.x == 0) {
-    for (int c = acc; c < N; ++c) path[c] = -1;
-    p.acc_len[b] = acc;
-    if (p.status) p.status[b] = status;
-    p.seq_count[b] = 0;
-  }
-  cluster_sync();
+  for (int c = (nonfin ? 0 : k); c < R; ++c) emitted[c] = -1;
+  if (p.tree)
+    for (int c = (nonfin ? 0 : acc); c < R; ++c) p.path[(size_t)b * R + c] = -1;
+  p.acc_len[b] = acc;
+  if (p.status) p.status[b] = status;
+  p.seq_count[b] = 0;
 }
 
 // ---------------------------------------------------------------- host side
 struct SampPlan {
   int CS, slice;
-  size_t smem;
+  size_t smem;  // bytes of one slice buffer
 };
 
 SampPlan plan_sampler(int V) {
@@ -925,10 +1149,14 @@ SampPlan plan_sampler(int V) {
   return pl;
 }
 
-size_t samp_ws(int B, int R, size_t* off_stats, size_t* off_cnt) {
+size_t dyn_smem(size_t slice_bytes) {
+  return 2 * slice_bytes + 3 * (size_t)kCandMax * (sizeof(uint64_t) + sizeof(float));
+}
+
+size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
   size_t off = sizeof(WsHeader);
-  *off_stats = off;
-  off += ((size_t)B * R * sizeof(RowStat) + 255) / 256 * 256;
+  *off_out = off;
+  off += ((size_t)B * R * sizeof(Outcome) + 255) / 256 * 256;
   *off_cnt = off;
   off += ((size_t)B * sizeof(int32_t) + 255) / 256 * 256;
   return off;
@@ -941,14 +1169,14 @@ spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
   static bool attr_set = false;  // once, at the largest size, so graph captures need no setup
   if (!attr_set) {
     if (cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kMaxSliceBytes) != cudaSuccess)
+                             (int)dyn_smem(kMaxSliceBytes)) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.CS, B * R, 1);
   cfg.blockDim = dim3(kST, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
+  cfg.dynamicSmemBytes = dyn_smem(pl.smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -983,13 +1211,14 @@ SP base_params(const float* logits, const float* q, const float* u, int B, int R
   prm.top_p = cfg->top_p;
   prm.greedy = cfg->greedy ? 1 : 0;
   prm.eos = cfg->eos_id;
-  size_t off_stats, off_cnt;
-  samp_ws(B, R, &off_stats, &off_cnt);
+  size_t off_out, off_cnt;
+  samp_ws(B, R, &off_out, &off_cnt);
   uint8_t* w = static_cast<uint8_t*>(ws);
   prm.err = reinterpret_cast<int32_t*>(w);
-  prm.stats = reinterpret_cast<RowStat*>(w + off_stats);
+  prm.outcomes = reinterpret_cast<Outcome*>(w + off_out);
   prm.seq_count = reinterpret_cast<int32_t*>(w + off_cnt);
   prm.bulk = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) ? 1 : 0;
+  prm.qbulk = (q && V % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0) ? 1 : 0;
   return prm;
 }
 

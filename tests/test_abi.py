@@ -109,7 +109,7 @@ def test_workspace_sizes(lib):
     assert sv.attn_workspace_size(1, 8, 32, 8, 128, 16, 513, 0) % 256 == 0
     # explicit splits are honoured up to the 64-token stage granularity
     assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193, 128) >= 128
-    assert sv.sample_workspace_size(4, 64, 128256) >= 256 + 4 * 64 * 32
+    assert sv.sample_workspace_size(4, 64, 128256) >= 256 + 4 * 64 * 16
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
