@@ -9,11 +9,13 @@ log-sum-exp combine) and the acceptance sampler.  Prints ONE JSON line.
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
 
 Timing: inputs resident in HBM; the step is captured once in a CUDA graph
-and replayed; L2 is flushed (a 2 x L2-size write) before every timed step,
-outside the timed events; each step is timed with CUDA events on its stream;
-K steps are bracketed by a barrier + synchronize; the max over ranks is
-reported.  The dominant kernel (the split-K partial pass) is timed with its
-own events inside the captured step for the roofline entry.
+and replayed; L2 is flushed before every timed step, outside the timed
+events: a 2 x L2-size write, then a 2 x L2-size read of another buffer so that
+the flush leaves no dirty lines whose write-back would land inside the step;
+each step is timed with CUDA events on its stream; K steps are bracketed by a
+barrier + synchronize; the max over ranks is reported.  The dominant kernel
+(the split-K partial pass) is timed with its own events inside the captured
+step for the roofline entry.
 """
 import argparse
 import hashlib
@@ -221,6 +223,11 @@ def bench_gpu(args, spec, ws, rank, local):
     ctx = step.w.ctx_len.cpu().numpy()
     nbytes = wl.algorithmic_bytes(spec, ctx)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush.zero_()           # evict the inputs: write more than L2 holds
+        clean.sum()             # then read more than L2 holds: write-backs finish here
     stream = torch.cuda.current_stream()
 
     for _ in range(3):                     # eager warm-up: attributes, descriptors
@@ -241,12 +248,12 @@ def bench_gpu(args, spec, ws, rank, local):
     step_ms, part_ms = [], []
     with ClockSampler(gpu_index) as clk:
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2()
             graph.replay()
         barrier(ws)
         torch.cuda.synchronize()
         for _ in range(args.steps):
-            flush.zero_()
+            flush_l2()
             e0.record(stream)
             graph.replay()
             e1.record(stream)
@@ -258,7 +265,7 @@ def bench_gpu(args, spec, ws, rank, local):
         barrier(ws)
         if ev_in is None:   # no graph event nodes: time the partial pass eagerly
             for _ in range(min(args.steps, 200)):
-                flush.zero_()
+                flush_l2()
                 e0.record(stream)
                 step.attn.partials()
                 e1.record(stream)
@@ -295,7 +302,8 @@ def bench_gpu(args, spec, ws, rank, local):
                 spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
                 step.w.block_table.shape[1], spec.num_splits),
             "sampler_dtype": "f32", "parallelism": f"replicas{ws}",
-            "l2": "flushed before every timed step (2 x L2 write, outside the timed events)",
+            "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read of a second "
+                  "buffer; outside the timed events)",
             "timing": "CUDA-graph replay, CUDA events per step"},
         "sequences_per_s": sum_over_ranks(spec.B, ws, device=dev) / (mean_ms_all * 1e-3),
         "step_hbm_gbs": step_gbs, "step_hbm_frac": step_gbs / peak,

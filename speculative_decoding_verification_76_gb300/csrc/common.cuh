@@ -166,6 +166,10 @@ SPEC_DEV unsigned long long dsmem_ld_u64(const void* local, uint32_t rank) {
   return v;
 }
 
+SPEC_DEV void dsmem_st_s32(void* local, uint32_t rank, int32_t v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(dsmem_addr(local, rank)), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- warp MMA (bf16)
 SPEC_DEV void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

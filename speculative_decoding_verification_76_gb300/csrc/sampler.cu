@@ -13,38 +13,56 @@
 //
 // GB300 design.  One thread-block cluster (up to 8 CTAs) per target row
 // holds that row in distributed shared memory: each CTA bulk-copies (TMA)
-// one slice of the vocabulary once; max, exp values, normaliser, the
-// top-k / top-p cut and the draws all run from shared memory, with
-// cluster-wide reductions gathered by one warp over DSMEM.  Every row
-// computes its own outcome independently (its draft test, and its
-// correction draw if it rejects; the last row's bonus draw; for a tree node
-// the first accepted child under the running residual, or its final draw),
-// so all B*R rows run at once and nothing waits on a serial walk.  The
-// cluster that finishes a sequence's last row assembles the outcomes.
+// one slice of the vocabulary once and replaces it in place by
+// E = exp((l - max)/T).  Every row computes its own outcome (its draft test,
+// and its correction draw if it rejects; the last row's bonus draw; for a
+// tree node the first accepted child under the running residual, or its
+// final draw), so all B*R rows run at once; the cluster that finishes a
+// sequence's last row assembles the outcomes.
 //
-// Numerics: exp((l - m)/T) is evaluated with the difference and quotient
-// carried in two floats (p matches a float64 evaluation to ~3e-7 relative);
-// sums are per-thread compensated and combined as float pairs in a fixed
-// order, so results are deterministic.  top-k / top-p: a 1/16-nat histogram
-// (below the row maximum) locates the crossing bin, its members are sorted
-// exactly by (logit desc, id asc); an exact radix selection is the fallback
-// for crossing bins too populous to sort.
+// The normaliser, the top-k / top-p cut and the draws need at most four
+// cluster exchanges per row:
+//   1. row maximum (and argmax, greedy);
+//   2. Z, and (truncation only) a histogram of E: 16 bins per octave of E
+//      (all E of a bin share one exponent), each holding its element count
+//      and the sum of its rounded 16-bit significands, which locates the
+//      bins the cut can fall in;
+//   3. (truncation only) the members of those bins, gathered and sorted by
+//      (logit desc, id asc) in every CTA, and the exact mass above them; the
+//      cut is found on exact integer masses (units of 2^-44);
+//   4. per-CTA sums of the draw weights; the CTA holding the crossing finds
+//      the token with one warp scan.
+// Values another CTA needs (E at a draft token, the residual at the next
+// child's token) travel in the exchange posts, so no CTA reads another's
+// vocabulary slice.  A crossing range too populous to sort (or a cut the
+// rounded bin masses placed one bin off) falls back to an exact radix
+// selection over the logit keys.  Shared-memory atomics are 32-bit only:
+// 64-bit and float atomics on shared memory are many times slower on sm_103.
+//
+// Numerics: exp((l - m)/T) = 2^x with x = (l - m) * (1/(T ln 2)) carried as
+// a float pair (Knuth's TwoSum for l - m, an FMA for the product error, the
+// constant split in two floats) and 2^x_hi * (1 + x_lo ln 2) on the
+// special-function unit; p matches a float64 evaluation to a few 1e-7.
 #include <algorithm>
 #include <climits>
+#include <cmath>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int kST = 512;
-constexpr int kSW = kST / 32;
 constexpr int kMaxCS = 8;
 constexpr int kMaxN = 64;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kCandMax = 1024;                 // sortable members of one crossing bin
-constexpr size_t kMaxSliceBytes = 84 * 1024;   // per CTA: logits + exp slices, each this size
+constexpr int kBins = 1024;                 // 32 per octave of E over 32 octaves; bin kBins: the rest
+constexpr int kHist = kBins + 1;
+constexpr int kHistPad = 1032;
+constexpr int kCandMax = 512;               // members of the crossing bins, whole cluster
+constexpr int kListPerCTA = 2048;           // kept positions listed per CTA (split over warps)
+constexpr size_t kMaxSliceBytes = 84 * 1024;
+constexpr float kLn2 = 0.6931471805599453f;
 
-// Outcome of one target row, written by its cluster.
+// Outcome of one target row, written by rank 0 of its cluster.
 struct Outcome {
   int32_t accept;  // chain: 1 if the row's draft is accepted; tree: accepted child or -1
   int32_t token;   // correction / bonus / final token of this row (-1 if none)
@@ -59,10 +77,10 @@ struct SP {
   const int32_t* parent;
   const float* u;
   int B, R, V, slice;
-  float T, invT;
+  float T, c_hi, c_lo;  // 1/(T ln 2) = c_hi + c_lo
   int top_k;
   float top_p;
-  int greedy, eos, tree, bulk, qbulk;
+  int greedy, eos, tree, bulk, qbulk, qsm;
   Outcome* outcomes;
   int32_t* seq_count;
   int32_t* err;
@@ -73,33 +91,42 @@ struct SP {
   int32_t* status;
 };
 
-struct alignas(16) Slot {
-  unsigned long long a, b;
+// One CTA's contribution to a cluster exchange (32 bytes).
+struct alignas(16) Post {
+  unsigned long long w[4];
 };
 
-struct DF {  // hi + lo, |lo| <= ulp(hi)/2
-  float hi, lo;
+SPEC_DEV unsigned long long f2w(float f) { return (unsigned long long)__float_as_uint(f); }
+SPEC_DEV float w2f(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+
+// The top-k / top-p cut.  Kept: key(l) > tau, or key == tau and id <= tie.
+// mode 0: no truncation; 1: decided through E (E > etau kept, E < etau not,
+// ties through the logit key); 2: through the logit key only.
+struct Cut {
+  int mode;
+  float etau;
+  uint32_t tau;
+  int tie;
 };
 
-struct Shared {
-  float red_f[kSW];
-  int red_i[kSW];
-  DF red_df[kSW];
-  Slot slots[4];
-  Slot gath[kMaxCS];
-  uint32_t hcnt[256];
-  float hmass[256];
-  uint32_t tcnt[256];
-  float tmass[256];
-  uint32_t rcnt[2][256];
-  unsigned long long rmass[2][256];
-  unsigned long long rtmass[256];
-  uint32_t rtcnt[256];
+template <int NW>
+struct Sh {
+  Post posts[2];
+  Post gath[kMaxCS];
+  float red_f[NW];
+  int red_i[NW];
+  float wsum[NW];
+  unsigned long long red_u[NW];
+  unsigned long long zk, zcut;
+  uint32_t oct[64];  // this CTA's per-octave counts [0, 32) and m16 sums [32, 64)
+  int list_n[NW];
   int bi[8];
-  DF bdf[2];
+  Cut cut;
   int par[kMaxN];
   int tok[kMaxN];
+  float invw_used[kMaxN];
   Outcome outs[kMaxN];
+  int token_in;
   uint64_t bar;
 };
 
@@ -111,144 +138,140 @@ SPEC_DEV uint32_t okey(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// exp((l - m) / T): the difference l - m (two-sum) and the quotient (FMA
-// remainder) are carried in two floats; exp(hi + lo) = exp(hi) * (1 + lo).
-SPEC_DEV float texp(float l, float m, float T, float invT) {
-  if (l == -INFINITY) return 0.f;
-  const float s = l - m;
-  const float bv = s - l;
-  const float av = s - bv;
-  const float e = (l - av) + (-m - bv);
-  const float qh = s * invT;
-  const float r = fmaf(-qh, T, s);
-  const float ql = (r + e) * invT;
-  return expf(qh) * (1.0f + ql);
-}
-
 SPEC_DEV bool is_kept(uint32_t key, int id, uint32_t tau, int tie) {
   return key > tau || (key == tau && id <= tie);
 }
 
-SPEC_DEV DF df_norm(float a, float b) {  // fast two-sum, |a| >= |b| or a == 0
-  const float s = a + b;
-  return DF{s, b - (s - a)};
+SPEC_DEV float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
-SPEC_DEV DF df_add(DF a, DF b) {
-  const float s = a.hi + b.hi;
-  const float bb = s - a.hi;
-  const float e = (a.hi - (s - bb)) + (b.hi - bb) + a.lo + b.lo;
-  return df_norm(s, e);
+SPEC_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-struct Kahan {
-  float s = 0.f, c = 0.f;
-  SPEC_DEV void add(float x) {
-    const float y = x - c;
-    const float t = s + y;
-    c = (t - s) - y;
-    s = t;
-  }
-  SPEC_DEV DF df() const { return df_norm(s, -c); }
-};
+// exp((l - m) / T) with nm = -m, lfloor = m - 150 T (below it E is 0 in float).
+SPEC_DEV float texp(float l, float nm, float lfloor, float c_hi, float c_lo) {
+  const float lc = fmaxf(l, lfloor);
+  const float s = __fadd_rn(lc, nm);
+  const float bv = __fsub_rn(s, lc);
+  const float av = __fsub_rn(s, bv);
+  const float e = __fadd_rn(__fsub_rn(lc, av), __fsub_rn(nm, bv));
+  const float xh = __fmul_rn(s, c_hi);
+  float xl = __fmaf_rn(s, c_hi, -xh);
+  xl = __fmaf_rn(s, c_lo, xl);
+  xl = __fmaf_rn(e, c_hi, xl);
+  const float y = ex2_approx(xh);
+  return __fmaf_rn(y, __fmul_rn(xl, kLn2), y);
+}
 
-SPEC_DEV double df_d(DF a) { return (double)a.hi + (double)a.lo; }
+// Histogram bin of E in [0, 1]: bins 0..1023 hold 32 per octave, all E of a
+// bin share one exponent (126 - b/32); bin 1024 holds the rest (E < 2^-32).
+SPEC_DEV int ebin(uint32_t bits) {
+  const int d = 0x3F7FFFFF - (int)bits;
+  return d < 0 ? 0 : min(d >> 18, kBins);
+}
 
-// ---------------------------------------------------------------- block reductions
-SPEC_DEV DF block_sum_df(DF v, Shared& sh) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// E rounded to a 16-bit significand, in units of 2^(-16 - b/32) of its bin b
+SPEC_DEV uint32_t m16(uint32_t bits) {
+  return bits >= 0x3F800000u ? 65536u : ((((bits & 0x7FFFFFu) | 0x800000u) + 128u) >> 8);
+}
+
+// a bin's sum of m16 in units of 2^-44
+SPEC_DEV unsigned long long bin_fx(unsigned long long m, int b) {
+  const int o = b >> 5;
+  return o <= 28 ? m << (28 - o) : m >> (o - 28);
+}
+
+// E (normal, <= 1) in units of 2^-44, exact for E >= 2^-20
+SPEC_DEV unsigned long long fx44(uint32_t bits) {
+  const int f = (int)(bits >> 23);
+  if (f == 0) return 0ull;
+  const unsigned long long sig = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = f - 106;
+  return sh >= 0 ? sig << sh : (sh > -24 ? sig >> (-sh) : 0ull);
+}
+
+constexpr double kFx = 17592186044416.0;  // 2^44
+
+SPEC_DEV float residual_w(float v, float invw, float qv) {
+  return fmaxf(__fmaf_rn(v, invw, -qv), 0.f);
+}
+
+// (h, l) += (ah, al) in float pairs (TwoSum), fixed order
+SPEC_DEV void df_acc(float& h, float& l, float ah, float al) {
+  const float s = __fadd_rn(h, ah);
+  const float bb = __fsub_rn(s, h);
+  const float e = __fadd_rn(__fadd_rn(__fsub_rn(h, __fsub_rn(s, bb)), __fsub_rn(ah, bb)),
+                            __fadd_rn(l, al));
+  h = __fadd_rn(s, e);
+  l = __fsub_rn(e, __fsub_rn(h, s));
+}
+
+// ---------------------------------------------------------------- block / cluster plumbing
+template <int NT>
+SPEC_DEV float block_sum_f(float v, Sh<NT / 32>& sh) {  // fixed order
+  constexpr int NW = NT / 32;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    v = df_add(v, DF{__shfl_xor_sync(kFull, v.hi, o), __shfl_xor_sync(kFull, v.lo, o)});
-  if (lane == 0) sh.red_df[w] = v;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if ((threadIdx.x & 31) == 0) sh.red_f[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (w == 0) {
-    DF x = lane < kSW ? sh.red_df[lane] : DF{0.f, 0.f};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      x = df_add(x, DF{__shfl_xor_sync(kFull, x.hi, o), __shfl_xor_sync(kFull, x.lo, o)});
-    if (lane == 0) sh.bdf[0] = x;
-  }
-  __syncthreads();
-  const DF t = sh.bdf[0];
+  float t = 0.f;
+  for (int i = 0; i < NW; ++i) t += sh.red_f[i];
   __syncthreads();
   return t;
 }
 
-// (max value, lowest id among maxima)
-SPEC_DEV void block_max_arg(float& v, int& id, Shared& sh) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+template <int NT>
+SPEC_DEV unsigned long long block_sum_u64(unsigned long long v, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(kFull, v, o);
-    const int oi = __shfl_xor_sync(kFull, id, o);
-    if (ov > v || (ov == v && oi < id)) {
-      v = ov;
-      id = oi;
-    }
-  }
-  if (lane == 0) {
-    sh.red_f[w] = v;
-    sh.red_i[w] = id;
-  }
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if ((threadIdx.x & 31) == 0) sh.red_u[threadIdx.x >> 5] = v;
   __syncthreads();
-  v = sh.red_f[0];
-  id = sh.red_i[0];
-  for (int i = 1; i < kSW; ++i) {
-    const float ov = sh.red_f[i];
-    const int oi = sh.red_i[i];
-    if (ov > v || (ov == v && oi < id)) {
-      v = ov;
-      id = oi;
-    }
-  }
-  __syncthreads();
-}
-
-SPEC_DEV int block_or(int v, Shared& sh) {
-  v = __reduce_or_sync(kFull, (unsigned)v);
-  if ((threadIdx.x & 31) == 0) sh.red_i[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int t = 0;
-  for (int i = 0; i < kSW; ++i) t |= sh.red_i[i];
+  unsigned long long t = 0;
+  for (int i = 0; i < NW; ++i) t += sh.red_u[i];
   __syncthreads();
   return t;
 }
 
-SPEC_DEV int block_min_i(int v, Shared& sh) {
+// inclusive scan over the CTA's threads (thread order), exact
+template <int NT>
+SPEC_DEV unsigned long long block_incl_scan_u64(unsigned long long v, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) sh.red_u[w] = v;
+  __syncthreads();
+  unsigned long long base = 0;
+  for (int i = 0; i < w && i < NW; ++i) base += sh.red_u[i];
+  __syncthreads();
+  return base + v;
+}
+
+template <int NT>
+SPEC_DEV int block_min_i(int v, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
   v = __reduce_min_sync(kFull, v);
   if ((threadIdx.x & 31) == 0) sh.red_i[threadIdx.x >> 5] = v;
   __syncthreads();
   int t = INT_MAX;
-  for (int i = 0; i < kSW; ++i) t = min(t, sh.red_i[i]);
+  for (int i = 0; i < NW; ++i) t = min(t, sh.red_i[i]);
   __syncthreads();
   return t;
 }
 
-// exclusive scan of one float per thread (fixed order); *total = block total
-// computed the way the last thread's running value is.
-SPEC_DEV float block_excl_scan_f(float v, float* total, Shared& sh) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  float incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) sh.red_f[w] = incl;
-  __syncthreads();
-  float base = 0.f;
-  for (int i = 0; i < w; ++i) base += sh.red_f[i];
-  const float excl = base + (incl - v);
-  __syncthreads();
-  if (threadIdx.x == kST - 1) sh.red_f[0] = excl + v;
-  __syncthreads();
-  *total = sh.red_f[0];
-  __syncthreads();
-  return excl;
-}
-
-SPEC_DEV int block_excl_scan_i(int v, int* total, Shared& sh) {
+template <int NT>
+SPEC_DEV int block_excl_scan_i(int v, int* total, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -258,444 +281,346 @@ SPEC_DEV int block_excl_scan_i(int v, int* total, Shared& sh) {
   }
   if (lane == 31) sh.red_i[w] = incl;
   __syncthreads();
-  int base = 0;
-  for (int i = 0; i < w; ++i) base += sh.red_i[i];
+  int base = 0, all = 0;
+  for (int i = 0; i < NW; ++i) {
+    if (i < w) base += sh.red_i[i];
+    all += sh.red_i[i];
+  }
   __syncthreads();
-  if (threadIdx.x == kST - 1) sh.red_i[0] = base + incl;
-  __syncthreads();
-  *total = sh.red_i[0];
-  __syncthreads();
+  *total = all;
   return base + incl - v;
 }
 
-// ---------------------------------------------------------------- cluster exchange
-// Every CTA posts one Slot; warp 0 fetches all CS slots (lane r <- rank r)
-// into sh.gath, which every thread then reads locally.  Posting slots rotate
-// over four buffers so a slot is never rewritten before every reader is past
-// the next cluster barrier.
-SPEC_DEV void cluster_allgather(Slot mine, int CS, int& ph, Shared& sh) {
-  Slot* s = &sh.slots[ph & 3];
+// Every CTA posts one Post; afterwards sh.gath[r] holds rank r's post in
+// every CTA.  Two post buffers alternate: a buffer is rewritten only two
+// exchanges later, after every reader has passed the cluster barrier between.
+template <int NW>
+SPEC_DEV void exchange(const Post& mine, int CS, int& ph, Sh<NW>& sh) {
+  Post* s = &sh.posts[ph & 1];
   if (threadIdx.x == 0) *s = mine;
   cluster_sync();
   if ((int)threadIdx.x < CS) {
-    Slot r;
-    r.a = dsmem_ld_u64(&s->a, threadIdx.x);
-    r.b = dsmem_ld_u64(&s->b, threadIdx.x);
+    Post r;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r.w[j] = dsmem_ld_u64(&s->w[j], threadIdx.x);
     sh.gath[threadIdx.x] = r;
   }
   __syncthreads();
   ++ph;
 }
 
-SPEC_DEV Slot cluster_from(Slot mine, int src, int CS, int& ph, Shared& sh) {
-  cluster_allgather(mine, CS, ph, sh);
-  return sh.gath[src];
+SPEC_DEV bool cut_keeps(const Cut& c, float e, int id, const float* lrow_full) {
+  if (c.mode == 0) return true;
+  if (c.mode == 1) {
+    if (e > c.etau) return true;
+    if (e < c.etau) return false;
+  }
+  return is_kept(okey(__ldg(lrow_full + id)), id, c.tau, c.tie);
 }
 
-SPEC_DEV Slot slot_df(DF v) {
-  return Slot{(unsigned long long)__float_as_uint(v.hi), (unsigned long long)__float_as_uint(v.lo)};
-}
+// ---------------------------------------------------------------- kept-set iteration
+// Each warp owns one contiguous range of the slice; its kept positions are
+// either listed (per-warp list, ascending) or the whole range is walked.
+template <int NW>
+struct Items {
+  bool listed;
+  const uint16_t* lists;  // NW x (kListPerCTA / NW)
+  int r0, r1;             // this warp's range [r0, r1)
+  SPEC_DEV int count(const Sh<NW>& sh) const {
+    return listed ? sh.list_n[threadIdx.x >> 5] : r1 - r0;
+  }
+  SPEC_DEV int at(int j) const {
+    return listed ? (int)lists[(threadIdx.x >> 5) * (kListPerCTA / NW) + j] : r0 + j;
+  }
+};
 
-SPEC_DEV DF cluster_sum_df(DF v, int CS, int& ph, Shared& sh) {
-  cluster_allgather(slot_df(v), CS, ph, sh);
-  DF t{0.f, 0.f};
-  for (int r = 0; r < CS; ++r)
-    t = df_add(t, DF{__uint_as_float((uint32_t)sh.gath[r].a),
-                     __uint_as_float((uint32_t)sh.gath[r].b)});
+// Weights of the draw over this CTA's items: mode 0 uses buf as is, mode 1
+// replaces buf by max(0, buf * invw - q) first.  Leaves per-warp sums in
+// sh.wsum and returns the CTA total (fixed order).
+template <int NT>
+SPEC_DEV float weight_pass(float* buf, const Items<NT / 32>& it, int mode, float invw,
+                           const float* qlo, bool q_shared, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31;
+  const int cnt = it.count(sh);
+  float acc = 0.f;
+  int j = lane;
+  if (mode == 1) {
+    for (; j + 96 < cnt; j += 128) {  // four independent q loads in flight
+      int k[4];
+      float v[4], qv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        k[u] = it.at(j + 32 * u);
+        v[u] = buf[k[u]];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        qv[u] = v[u] > 0.f ? (q_shared ? qlo[k[u]] : __ldg(qlo + k[u])) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v[u] = residual_w(v[u], invw, qv[u]);
+        buf[k[u]] = v[u];
+        acc += v[u];
+      }
+    }
+  }
+  for (; j < cnt; j += 32) {
+    const int k = it.at(j);
+    float v = buf[k];
+    if (mode == 1) {
+      const float qv = v > 0.f ? (q_shared ? qlo[k] : __ldg(qlo + k)) : 0.f;
+      v = residual_w(v, invw, qv);
+      buf[k] = v;
+    }
+    acc += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+  if (lane == 0) sh.wsum[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < NW; ++w) t += sh.wsum[w];
   return t;
 }
 
-// ---------------------------------------------------------------- the slice
-struct Slice {
-  float* buf;  // shared memory, n floats
-  int lo, n;
-};
-
-// Load a row slice into shared memory (TMA bulk copy when aligned).
-SPEC_DEV void load_row(const SP& p, const float* row, Slice& sl, Shared& sh, uint32_t& bar_phase) {
-  __syncthreads();  // every reader of the previous contents is done
-  if (sl.n <= 0) return;
-  if (p.bulk) {
-    if (threadIdx.x == 0) {
-      fence_proxy_async();  // order earlier generic writes before the async copy
-      mbar_arrive_expect_tx(&sh.bar, (uint32_t)sl.n * 4u);
-      bulk_load(sl.buf, row + sl.lo, (uint32_t)sl.n * 4u, &sh.bar);
+// Weights of a chain draw over this warp's whole range [r0, r1) with the cut
+// applied inline: w = kept ? (mode 1: max(0, E * invw - q); mode 0: E) : 0,
+// written back to buf for the walk.  Per-warp sums in sh.wsum, CTA total
+// returned (fixed order).  r0 is a multiple of 4.
+template <int NT>
+SPEC_DEV float weight_full(float* buf, int r0, int r1, const Cut& cut, int lo,
+                           const float* lrow_full, int mode, float invw, const float* qlo,
+                           bool q_shared, bool q_vec, Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31;
+  const int r1v = r0 + ((r1 - r0) & ~3);
+  float acc = 0.f;
+  for (int k = r0 + 4 * lane; k < r1v; k += 128) {
+    float4 e4 = *reinterpret_cast<const float4*>(buf + k);
+    float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+    bool kp[4];
+    bool all = true, any = false;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      kp[u] = ev[u] > 0.f && cut_keeps(cut, ev[u], lo + k + u, lrow_full);
+      all &= kp[u];
+      any |= kp[u];
     }
-    mbar_wait(&sh.bar, bar_phase, p.err);
-    bar_phase ^= 1u;
-  } else {
-    for (int i = threadIdx.x; i < sl.n; i += kST) sl.buf[i] = row[sl.lo + i];
+    float qv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (mode == 1 && any) {
+      if (q_shared || (all && q_vec)) {
+        const float4 q4 = q_shared ? *reinterpret_cast<const float4*>(qlo + k)
+                                   : __ldg(reinterpret_cast<const float4*>(qlo + k));
+        qv[0] = q4.x;
+        qv[1] = q4.y;
+        qv[2] = q4.z;
+        qv[3] = q4.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) qv[u] = kp[u] ? __ldg(qlo + k + u) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = kp[u] ? (mode == 1 ? residual_w(ev[u], invw, qv[u]) : ev[u]) : 0.f;
+      ev[u] = w;
+      acc += w;
+    }
+    *reinterpret_cast<float4*>(buf + k) = make_float4(ev[0], ev[1], ev[2], ev[3]);
   }
+  for (int k = r1v + lane; k < r1; k += 32) {
+    const float e = buf[k];
+    const bool kp = e > 0.f && cut_keeps(cut, e, lo + k, lrow_full);
+    float w = 0.f;
+    if (kp) w = mode == 1 ? residual_w(e, invw, q_shared ? qlo[k] : __ldg(qlo + k)) : e;
+    buf[k] = w;
+    acc += w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+  if (lane == 0) sh.wsum[threadIdx.x >> 5] = acc;
   __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < NW; ++w) t += sh.wsum[w];
+  return t;
 }
 
-// coarse bin of a logit: 1/16 nat below the row maximum, 255 = beyond 16 nats
-SPEC_DEV int coarse_bin(float l, float m, float scale16) {
-  const float d = (m - l) * scale16;  // monotone non-increasing in l
-  return d < 255.f ? (int)d : 255;
-}
-
-// Deterministic cluster sum of E over the elements with pred(k).
-template <class Pred>
-SPEC_DEV DF cluster_masked_sum(const Slice& sl, const float* E, Pred pred, int CS, int& ph,
-                               Shared& sh) {
-  Kahan acc;
-  for (int k = threadIdx.x; k < sl.n; k += kST)
-    if (pred(k)) acc.add(E[k]);
-  return cluster_sum_df(block_sum_df(acc.df(), sh), CS, ph, sh);
-}
-
-// First index d in [0, n) (n <= 256) where the running sum of val[0..d]
-// reaches target; -1 if none.  Warp 0 scans 8 bins per lane; the result is
-// broadcast to the block.
-template <class T>
-SPEC_DEV int first_reaching(const T* val, int n, double target, Shared& sh) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    double ls = 0.0;
-    for (int j = 0; j < 8; ++j)
-      if (8 * lane + j < n) ls += (double)val[8 * lane + j];
-    double incl = ls;
+// After the exchange of CTA totals (post word 0): the draw's owner CTA finds
+// the first item whose running weight (ascending id over the cluster)
+// exceeds u * W and returns its id; other CTAs return -1; -2 if W == 0
+// (same in every CTA).  The owner warp splits its items into one contiguous
+// chunk per lane, scans the chunk sums and walks the one chunk that crosses.
+template <int NT>
+SPEC_DEV int locate(const float* buf, const Items<NT / 32>& it, int lo, float u, int rank, int CS,
+                    Sh<NT / 32>& sh) {
+  constexpr int NW = NT / 32;
+  float W = 0.f;
+  for (int r = 0; r < CS; ++r) W += w2f(sh.gath[r].w[0]);
+  if (!(W > 0.f)) return -2;
+  const float target = u * W;
+  int owner = -1, last_nz = -1;
+  float pre = 0.f, pre_owner = 0.f, pre_last = 0.f;
+  for (int r = 0; r < CS; ++r) {
+    const float t = w2f(sh.gath[r].w[0]);
+    if (t > 0.f) {
+      if (owner < 0 && pre + t > target) {
+        owner = r;
+        pre_owner = pre;
+      }
+      last_nz = r;
+      pre_last = pre;
+    }
+    pre += t;
+  }
+  if (owner < 0) {
+    owner = last_nz;
+    pre_owner = pre_last;
+  }
+  if (owner != rank) return -1;
+  int ow = -1, lw = -1;
+  float wpre = pre_owner, base_ow = 0.f, base_lw = 0.f;
+  for (int w = 0; w < NW; ++w) {
+    const float t = sh.wsum[w];
+    if (t > 0.f) {
+      if (ow < 0 && wpre + t > target) {
+        ow = w;
+        base_ow = wpre;
+      }
+      lw = w;
+      base_lw = wpre;
+    }
+    wpre += t;
+  }
+  if (ow < 0) {
+    ow = lw;
+    base_ow = base_lw;
+  }
+  if (ow < 0) return -1;  // unreachable: the owner CTA has positive weight
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == ow) {
+    const int cnt = it.count(sh);
+    const int c = ((cnt + 31) / 32) | 1;  // odd chunk length: conflict-free shared reads
+    const int j0 = min(lane * c, cnt), j1 = min(j0 + c, cnt);
+    float ls = 0.f;
+    for (int j = j0; j < j1; ++j) ls += buf[it.at(j)];
+    const float tw = target - base_ow;  // the crossing, relative to the warp's start
+    float incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double t = __shfl_up_sync(kFull, incl, o);
+      const float t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
-    const unsigned hit = __ballot_sync(kFull, incl >= target);
-    int res = -1;
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      if (lane == L) {
-        double cum = incl - ls;
-        for (int j = 0; j < 8; ++j) {
-          const int d = 8 * L + j;
-          if (d >= n) break;
-          cum += (double)val[d];
-          if (cum >= target) {
-            res = d;
+    const unsigned hit = __ballot_sync(kFull, ls > 0.f && incl > tw);
+    const unsigned nz = __ballot_sync(kFull, ls > 0.f);
+    const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
+    int found = -1;
+    if (lane == L) {
+      const float tl = tw - (incl - ls);  // relative to this lane's chunk
+      float run = 0.f;
+      int lastk = -1;
+      for (int j = j0; j < j1; ++j) {
+        const int k = it.at(j);
+        const float v = buf[k];
+        if (v > 0.f) {
+          lastk = k;
+          run += v;
+          if (run > tl) {
+            found = k;
             break;
           }
         }
       }
-      res = __shfl_sync(kFull, res, L);
+      if (found < 0) found = lastk;  // rounding left the crossing just past the end
     }
-    if (lane == 0) sh.bi[2] = res;
+    found = __shfl_sync(kFull, found, L < 0 ? 0 : L);
+    if (lane == 0) sh.bi[7] = (L < 0 || found < 0) ? INT_MAX : lo + found;
   }
   __syncthreads();
-  const int r = sh.bi[2];
+  const int t = sh.bi[7];
   __syncthreads();
-  return r;
-}
-
-// ---------------------------------------------------------------- crossing-bin sort
-SPEC_DEV uint64_t cand_of(float l, int id) {
-  return ((uint64_t)okey(l) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)id);
-}
-SPEC_DEV uint32_t cand_key(uint64_t c) { return (uint32_t)(c >> 32); }
-SPEC_DEV int cand_id(uint64_t c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
-
-struct Scratch {
-  uint64_t *cand, *gk, *sk;
-  float *candE, *ge, *se;
-};
-
-struct Sorted {
-  uint64_t* key;  // CTA 0: members sorted by (logit desc, id asc)
-  float* E;       // their exp values, same order
-  int n;
-};
-
-// Gather the elements with pred(k) (with their exp values) from every CTA
-// into CTA 0 and rank-sort them there.  The caller guarantees the cluster
-// count is <= kCandMax.  Same n in every CTA; keys valid in CTA 0 only.
-template <class Pred>
-SPEC_DEV Sorted gather_sort(const Slice& sl, const float* E, const Scratch& sc, Pred pred, int rank,
-                            int CS, int& ph, Shared& sh) {
-  if (threadIdx.x == 0) sh.bi[1] = 0;
-  __syncthreads();
-  for (int k = threadIdx.x; k < sl.n; k += kST) {
-    if (pred(k)) {
-      const int slot = atomicAdd(&sh.bi[1], 1);
-      if (slot < kCandMax) {
-        sc.cand[slot] = cand_of(sl.buf[k], sl.lo + k);
-        sc.candE[slot] = E[k];
-      }
-    }
-  }
-  __syncthreads();
-  const int mine = min(sh.bi[1], kCandMax);
-  cluster_allgather(Slot{(unsigned long long)mine, 0ull}, CS, ph, sh);
-  int cnt[kMaxCS];
-  int total = 0;
-  for (int r = 0; r < CS; ++r) {
-    cnt[r] = (int)sh.gath[r].a;
-    total += cnt[r];
-  }
-  total = min(total, kCandMax);
-  if (rank == 0) {
-    int off = 0;
-    for (int r = 0; r < CS; ++r) {
-      for (int j = threadIdx.x; j < cnt[r] && off + j < kCandMax; j += kST) {
-        sc.gk[off + j] = dsmem_ld_u64(&sc.cand[j], r);
-        sc.ge[off + j] = dsmem_ld_f32(&sc.candE[j], r);
-      }
-      off += cnt[r];
-    }
-    __syncthreads();
-    // rank sort: keys are distinct (ids are), rank = number of larger keys
-    for (int i = threadIdx.x; i < total; i += kST) {
-      const uint64_t c = sc.gk[i];
-      int rk = 0;
-      for (int j = 0; j < total; ++j) rk += sc.gk[j] > c ? 1 : 0;
-      sc.sk[rk] = c;
-      sc.se[rk] = sc.ge[i];
-    }
-    __syncthreads();
-  }
-  cluster_sync();  // other CTAs' candidate lists stay intact until CTA 0 has copied them
-  return Sorted{sc.sk, sc.se, total};
-}
-
-// In CTA 0: the first sorted index j whose base + sum(E[0..j]) reaches thr
-// (float-pair sums, fixed order), with that running sum; (-1, 0) if none.
-SPEC_DEV void sorted_crossing(const Sorted& so, DF base, double thr, int* idx, DF* at, Shared& sh) {
-  const int per = (so.n + kST - 1) / kST;
-  const int s0 = min((int)threadIdx.x * per, so.n), s1 = min(s0 + per, so.n);
-  DF run{0.f, 0.f};
-  for (int j = s0; j < s1; ++j) run = df_add(run, DF{so.E[j], 0.f});
-  // inclusive scan over the lanes, then over the warps, in a fixed order
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  DF incl = run;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const DF t = DF{__shfl_up_sync(kFull, incl.hi, o), __shfl_up_sync(kFull, incl.lo, o)};
-    if (lane >= o) incl = df_add(t, incl);
-  }
-  const DF lanes_before = DF{__shfl_up_sync(kFull, incl.hi, 1), __shfl_up_sync(kFull, incl.lo, 1)};
-  if (lane == 31) sh.red_df[w] = incl;
-  __syncthreads();
-  DF excl = base;
-  for (int i = 0; i < w; ++i) excl = df_add(excl, sh.red_df[i]);
-  if (lane > 0) excl = df_add(excl, lanes_before);
-  __syncthreads();
-  int found = INT_MAX;
-  DF val{0.f, 0.f};
-  if (df_d(df_add(excl, run)) >= thr) {
-    DF acc = excl;
-    for (int j = s0; j < s1; ++j) {
-      acc = df_add(acc, DF{so.E[j], 0.f});
-      if (df_d(acc) >= thr) {
-        found = j;
-        val = acc;
-        break;
-      }
-    }
-  }
-  const int f = block_min_i(found, sh);
-  if (found == f && f != INT_MAX) sh.bdf[1] = val;
-  __syncthreads();
-  *idx = (f == INT_MAX) ? -1 : f;
-  *at = (f == INT_MAX) ? DF{0.f, 0.f} : sh.bdf[1];
-  __syncthreads();
-}
-
-// In CTA 0: float-pair sum (fixed order) of the first n sorted exp values.
-SPEC_DEV DF sorted_head_sum(const Sorted& so, int n, Shared& sh) {
-  const int per = (n + kST - 1) / kST;
-  const int s0 = min((int)threadIdx.x * per, n), s1 = min(s0 + per, n);
-  DF run{0.f, 0.f};
-  for (int j = s0; j < s1; ++j) run = df_add(run, DF{so.E[j], 0.f});
-  return block_sum_df(run, sh);
-}
-
-struct Trunc {
-  uint32_t tau;
-  int tie;
-  DF Z;
-  bool ok;
-};
-
-// Top-k then top-p by coarse bins + an exact sort of the crossing bin.
-// ok = false when a crossing bin is too populous (the caller falls back to
-// the exact radix selection).
-SPEC_DEV Trunc truncate_fast(const SP& p, const Slice& sl, const float* E, const Scratch& sc,
-                             float m, DF Zall, int rank, int CS, int& ph, Shared& sh) {
-  Trunc tr{0u, INT_MAX, Zall, true};
-  const float s16 = p.invT * 16.f;
-  for (int d = threadIdx.x; d < 256; d += kST) {
-    sh.hcnt[d] = 0u;
-    sh.hmass[d] = 0.f;
-  }
-  __syncthreads();
-  for (int k = threadIdx.x; k < sl.n; k += kST) {
-    const int bn = coarse_bin(sl.buf[k], m, s16);
-    if (bn < 255) {
-      atomicAdd(&sh.hcnt[bn], 1u);
-      atomicAdd(&sh.hmass[bn], E[k]);
-    }
-  }
-  __syncthreads();
-  cluster_sync();
-  // cluster totals: thread d sums bin d over the ranks
-  for (int d = threadIdx.x; d < 256; d += kST) {
-    uint32_t c = 0;
-    float mm = 0.f;
-    for (int r = 0; r < CS; ++r) {
-      c += dsmem_ld_u32(&sh.hcnt[d], r);
-      mm += dsmem_ld_f32(&sh.hmass[d], r);
-    }
-    sh.tcnt[d] = c;
-    sh.tmass[d] = mm;
-  }
-  __syncthreads();
-  int bk = 254;  // last bin (partly) kept by top-k
-  if (p.top_k > 0 && p.top_k < p.V) {
-    const int bsel = first_reaching(sh.tcnt, 255, (double)p.top_k, sh);
-    if (bsel < 0 || sh.tcnt[bsel] > (uint32_t)kCandMax) {
-      tr.ok = false;
-      return tr;
-    }
-    uint32_t above_cnt = 0;
-    for (int d = 0; d < bsel; ++d) above_cnt += sh.tcnt[d];
-    const int need = p.top_k - (int)above_cnt;
-    const DF above = cluster_masked_sum(
-        sl, E, [&](int k) { return coarse_bin(sl.buf[k], m, s16) < bsel; }, CS, ph, sh);
-    const Sorted so = gather_sort(
-        sl, E, sc, [&](int k) { return coarse_bin(sl.buf[k], m, s16) == bsel; }, rank, CS, ph, sh);
-    const int nn = min(need, so.n);
-    Slot mine{0ull, 0ull};
-    if (rank == 0) {
-      const DF part = sorted_head_sum(so, nn, sh);
-      if (threadIdx.x == 0) mine = Slot{so.key[nn - 1], slot_df(part).a | (slot_df(part).b << 32)};
-    }
-    const Slot o = cluster_from(mine, 0, CS, ph, sh);
-    const DF part = DF{__uint_as_float((uint32_t)o.b), __uint_as_float((uint32_t)(o.b >> 32))};
-    tr.tau = cand_key(o.a);
-    tr.tie = cand_id(o.a);
-    tr.Z = df_add(above, part);
-    bk = bsel;
-  }
-  if (p.top_p > 0.f && p.top_p < 1.f) {
-    const double thr = (double)p.top_p * df_d(tr.Z);
-    const uint32_t tk = tr.tau;
-    const int tc = tr.tie;
-    int bp = first_reaching(sh.tmass, bk + 1, thr, sh);
-    if (bp < 0) bp = bk;
-    for (int attempt = 0; attempt < 6; ++attempt) {
-      if (bp < 0 || bp > bk || sh.tcnt[bp] > (uint32_t)kCandMax) break;
-      const int bsel = bp;
-      const DF above = cluster_masked_sum(
-          sl, E,
-          [&](int k) {
-            const float l = sl.buf[k];
-            return coarse_bin(l, m, s16) < bsel && is_kept(okey(l), sl.lo + k, tk, tc);
-          },
-          CS, ph, sh);
-      if (df_d(above) >= thr) {  // the crossing lies in an earlier bin
-        --bp;
-        continue;
-      }
-      const Sorted so = gather_sort(
-          sl, E, sc,
-          [&](int k) {
-            const float l = sl.buf[k];
-            return coarse_bin(l, m, s16) == bsel && is_kept(okey(l), sl.lo + k, tk, tc);
-          },
-          rank, CS, ph, sh);
-      Slot mine{~0ull, 0ull};
-      if (rank == 0) {
-        int idx;
-        DF at;
-        sorted_crossing(so, above, thr, &idx, &at, sh);
-        if (threadIdx.x == 0 && idx >= 0)
-          mine = Slot{so.key[idx], slot_df(at).a | (slot_df(at).b << 32)};
-      }
-      const Slot o = cluster_from(mine, 0, CS, ph, sh);
-      if (o.a == ~0ull) {  // not in this bin: move on to the next one
-        ++bp;
-        continue;
-      }
-      tr.tau = cand_key(o.a);
-      tr.tie = cand_id(o.a);
-      tr.Z = DF{__uint_as_float((uint32_t)o.b), __uint_as_float((uint32_t)(o.b >> 32))};
-      return tr;
-    }
-    tr.ok = false;
-  }
-  return tr;
+  return t == INT_MAX ? -1 : t;
 }
 
 // ---------------------------------------------------------------- exact radix fallback
-// Radix selection, most significant digit first, of the position in
-// (key desc, id asc) order where the running weight reaches the target.
-// Weight = 1 per element (top-k) or its 2^-40 fixed-point mass (top-p).
+// Radix selection over the logit keys (read from global memory), most
+// significant digit first, of the position in (key desc, id asc) order where
+// the running weight reaches the target.  Weight = 1 per element (top-k) or
+// its 2^-40 fixed-point E (top-p).  Scratch: rcnt[2][256] u32,
+// rmass[2][256] u64, rtmass[256] u64, rtcnt[256] u32.
+struct RadixScratch {
+  uint32_t* rcnt;
+  unsigned long long* rmass;
+  unsigned long long* rtmass;
+  uint32_t* rtcnt;
+};
+
 struct Sel {
   uint32_t tau;
   unsigned long long above, at_weight, target;
   uint32_t at_count;
 };
 
-template <class Keep, class Weight>
-SPEC_DEV Sel radix_select(const Slice& sl, bool target_is_fraction, double frac,
-                          unsigned long long target_abs, Keep keep, Weight weight, int CS, int& ph,
-                          Shared& sh) {
+template <int NT, class Keep, class Weight>
+SPEC_DEV Sel radix_select(const float* lrow, int n, bool target_is_fraction, double frac,
+                          unsigned long long target_abs, Keep keep, Weight weight,
+                          const RadixScratch& rs, int CS) {
   uint32_t prefix = 0, pmask = 0;
   unsigned long long above = 0, target = target_abs;
   Sel out{};
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int h = pass & 1;
-    for (int i = threadIdx.x; i < 256; i += kST) {
-      sh.rmass[h][i] = 0ull;
-      sh.rcnt[h][i] = 0u;
+    for (int i = threadIdx.x; i < 256; i += NT) {
+      rs.rmass[h * 256 + i] = 0ull;
+      rs.rcnt[h * 256 + i] = 0u;
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < sl.n; k += kST) {
-      const uint32_t key = okey(sl.buf[k]);
+    for (int k = threadIdx.x; k < n; k += NT) {
+      const uint32_t key = okey(__ldg(lrow + k));
       if ((key & pmask) == prefix && keep(k, key)) {
         const uint32_t digit = (key >> shift) & 255u;
-        atomicAdd(&sh.rcnt[h][digit], 1u);
-        atomicAdd(&sh.rmass[h][digit], weight(k));
+        atomicAdd(&rs.rcnt[h * 256 + digit], 1u);
+        atomicAdd(&rs.rmass[h * 256 + digit], weight(k));
       }
     }
     __syncthreads();
     cluster_sync();
-    for (int d = threadIdx.x; d < 256; d += kST) {
+    for (int d = threadIdx.x; d < 256; d += NT) {
       unsigned long long mm = 0;
       uint32_t c = 0;
       for (int r = 0; r < CS; ++r) {
-        mm += dsmem_ld_u64(&sh.rmass[h][d], r);
-        c += dsmem_ld_u32(&sh.rcnt[h][d], r);
+        mm += dsmem_ld_u64(&rs.rmass[h * 256 + d], r);
+        c += dsmem_ld_u32(&rs.rcnt[h * 256 + d], r);
       }
-      sh.rtmass[255 - d] = mm;  // descending digit order
-      sh.rtcnt[255 - d] = c;
+      rs.rtmass[255 - d] = mm;  // descending digit order
+      rs.rtcnt[255 - d] = c;
     }
     __syncthreads();
     if (pass == 0 && target_is_fraction) {
       unsigned long long tot = 0;
-      for (int d = 0; d < 256; ++d) tot += sh.rtmass[d];
+      for (int d = 0; d < 256; ++d) tot += rs.rtmass[d];
       const double thr = ceil(frac * (double)tot);
       target = thr < 1.0 ? 1ull : (unsigned long long)thr;
       if (target > tot) target = tot;
     }
-    // first descending digit whose running weight reaches target - above
     const unsigned long long need = target - above;
     unsigned long long cum = 0;
     int sel = 255;
     for (int d = 0; d < 256; ++d) {  // every thread, identical result
-      if (cum + sh.rtmass[d] >= need) {
+      if (cum + rs.rtmass[d] >= need) {
         sel = d;
         break;
       }
-      cum += sh.rtmass[d];
+      cum += rs.rtmass[d];
     }
     above += cum;
     const uint32_t digit = 255u - (uint32_t)sel;
     prefix |= digit << shift;
     pmask |= 255u << shift;
     if (pass == 3) {
-      out.at_count = sh.rtcnt[sel];
-      out.at_weight = sh.rtmass[sel];
+      out.at_count = rs.rtcnt[sel];
+      out.at_weight = rs.rtmass[sel];
     }
     __syncthreads();
   }
@@ -705,21 +630,21 @@ SPEC_DEV Sel radix_select(const Slice& sl, bool target_is_fraction, double frac,
   return out;
 }
 
-// The id (global) of the nth (1-based) element, in ascending id order over
-// the cluster, for which pred(local index) holds.  Same result in all CTAs.
-template <class Pred>
-SPEC_DEV int nth_in_cluster(const Slice& sl, int nth, Pred pred, int rank, int CS, int& ph,
-                            Shared& sh) {
-  const int seg = (sl.n + kST - 1) / kST;
-  const int s0 = min((int)threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
+// The id of the nth (1-based) element, in ascending id order over the
+// cluster, for which pred(local index) holds.  Same result in all CTAs.
+template <int NT, class Pred>
+SPEC_DEV int nth_in_cluster(int n, int lo, int nth, Pred pred, int rank, int CS, int& ph,
+                            Sh<NT / 32>& sh) {
+  const int seg = (n + NT - 1) / NT;
+  const int s0 = min((int)threadIdx.x * seg, n), s1 = min(s0 + seg, n);
   int c = 0;
   for (int k = s0; k < s1; ++k) c += pred(k) ? 1 : 0;
   int tot;
-  const int excl = block_excl_scan_i(c, &tot, sh);
-  cluster_allgather(Slot{(unsigned long long)tot, 0ull}, CS, ph, sh);
+  const int excl = block_excl_scan_i<NT>(c, &tot, sh);
+  exchange(Post{{(unsigned long long)tot, 0ull, 0ull, 0ull}}, CS, ph, sh);
   int before = 0, owner = -1;
   for (int r = 0; r < CS; ++r) {
-    const int tr = (int)sh.gath[r].a;
+    const int tr = (int)sh.gath[r].w[0];
     if (owner < 0 && before + tr >= nth) owner = r;
     if (owner < 0) before += tr;
   }
@@ -730,45 +655,43 @@ SPEC_DEV int nth_in_cluster(const Slice& sl, int nth, Pred pred, int rank, int C
       int cnt = excl;
       for (int k = s0; k < s1; ++k)
         if (pred(k) && ++cnt == local) {
-          found = sl.lo + k;
+          found = lo + k;
           break;
         }
     }
   }
-  found = block_min_i(found, sh);
-  const Slot o = cluster_from(Slot{(unsigned long long)(unsigned)found, 0ull},
-                              owner < 0 ? 0 : owner, CS, ph, sh);
-  return owner < 0 ? INT_MAX : (int)(unsigned)o.a;
+  found = block_min_i<NT>(found, sh);
+  exchange(Post{{(unsigned long long)(unsigned)found, 0ull, 0ull, 0ull}}, CS, ph, sh);
+  return owner < 0 ? INT_MAX : (int)(unsigned)sh.gath[owner].w[0];
 }
 
-SPEC_DEV Trunc truncate_radix(const SP& p, const Slice& sl, float m, int rank, int CS, int& ph,
-                              Shared& sh) {
-  Trunc tr{0u, INT_MAX, DF{0.f, 0.f}, true};
-  cluster_sync();  // other CTAs may still read this CTA's coarse histogram
+// tau / tie of the top-k then top-p cut by exact radix selection; E in buf.
+template <int NT>
+SPEC_DEV Cut cut_radix(const SP& p, const float* lrow, const float* buf, int n, int lo,
+                       const RadixScratch& rs, int rank, int CS, int& ph, Sh<NT / 32>& sh) {
+  Cut c{2, 0.f, 0u, INT_MAX};
   if (p.top_k > 0 && p.top_k < p.V) {
-    const Sel s = radix_select(
-        sl, false, 0.0, (unsigned long long)p.top_k, [](int, uint32_t) { return true; },
-        [](int) { return 1ull; }, CS, ph, sh);
+    const Sel s = radix_select<NT>(
+        lrow, n, false, 0.0, (unsigned long long)p.top_k, [](int, uint32_t) { return true; },
+        [](int) { return 1ull; }, rs, CS);
     const int need = (int)(s.target - s.above);
-    tr.tau = s.tau;
+    c.tau = s.tau;
     if ((uint32_t)need >= s.at_count) {
-      tr.tie = INT_MAX;
+      c.tie = INT_MAX;
     } else {
       const uint32_t tau = s.tau;
-      tr.tie = nth_in_cluster(
-          sl, need, [&](int k) { return okey(sl.buf[k]) == tau; }, rank, CS, ph, sh);
+      c.tie = nth_in_cluster<NT>(
+          n, lo, need, [&](int k) { return okey(__ldg(lrow + k)) == tau; }, rank, CS, ph, sh);
     }
   }
   if (p.top_p > 0.f && p.top_p < 1.f) {
-    const uint32_t tk = tr.tau;
-    const int tc = tr.tie;
-    const float T = p.T, invT = p.invT;
-    auto keep_k = [&](int k, uint32_t key) { return is_kept(key, sl.lo + k, tk, tc); };
+    const uint32_t tk = c.tau;
+    const int tc = c.tie;
+    auto keep_k = [&](int k, uint32_t key) { return is_kept(key, lo + k, tk, tc); };
     auto mass = [&](int k) {
-      const float e = texp(sl.buf[k], m, T, invT);
-      return (unsigned long long)__float2ull_rn(e * 1099511627776.0f);  // 2^40
+      return (unsigned long long)__float2ull_rn(buf[k] * 1099511627776.0f);  // 2^40
     };
-    const Sel s = radix_select(sl, true, (double)p.top_p, 0ull, keep_k, mass, CS, ph, sh);
+    const Sel s = radix_select<NT>(lrow, n, true, (double)p.top_p, 0ull, keep_k, mass, rs, CS);
     const unsigned long long e_tau = s.at_count ? s.at_weight / s.at_count : 0ull;
     unsigned long long need = 1;
     if (e_tau > 0 && s.target > s.above) need = (s.target - s.above + e_tau - 1) / e_tau;
@@ -779,74 +702,25 @@ SPEC_DEV Trunc truncate_radix(const SP& p, const Slice& sl, float m, int rank, i
     if (need == s.at_count) {
       tie = (tau == tk) ? tc : INT_MAX;
     } else {
-      tie = nth_in_cluster(
-          sl, (int)need,
+      tie = nth_in_cluster<NT>(
+          n, lo, (int)need,
           [&](int k) {
-            const uint32_t key = okey(sl.buf[k]);
-            return key == tau && is_kept(key, sl.lo + k, tk, tc);
+            const uint32_t key = okey(__ldg(lrow + k));
+            return key == tau && is_kept(key, lo + k, tk, tc);
           },
           rank, CS, ph, sh);
     }
-    tr.tau = tau;
-    tr.tie = tie;
+    c.tau = tau;
+    c.tie = tie;
   }
-  return tr;
+  return c;
 }
 
-// ---------------------------------------------------------------- the draw
-// The first id whose running sum (ascending id order over the cluster) of
-// the slice values exceeds u * total; -2 if the total is zero.  Same result
-// in all CTAs.
-SPEC_DEV int draw_from_slice(const Slice& sl, float u, int rank, int CS, int& ph, Shared& sh) {
-  const int seg = (sl.n + kST - 1) / kST;
-  const int s0 = min((int)threadIdx.x * seg, sl.n), s1 = min(s0 + seg, sl.n);
-  float run = 0.f;
-  for (int k = s0; k < s1; ++k) run += sl.buf[k];
-  float tot;
-  const float excl = block_excl_scan_f(run, &tot, sh);
-  cluster_allgather(Slot{(unsigned long long)__float_as_uint(tot), 0ull}, CS, ph, sh);
-  float pre[kMaxCS + 1], tots[kMaxCS];
-  pre[0] = 0.f;
-  for (int r = 0; r < CS; ++r) {
-    tots[r] = __uint_as_float((uint32_t)sh.gath[r].a);
-    pre[r + 1] = pre[r] + tots[r];
-  }
-  const float W = pre[CS];
-  if (!(W > 0.f)) return -2;
-  const float target = u * W;
-  int owner = -1;
-  for (int r = 0; r < CS; ++r)
-    if (owner < 0 && tots[r] > 0.f && pre[r] + tots[r] > target) owner = r;
-  if (owner < 0)
-    for (int r = CS - 1; r >= 0; --r)
-      if (owner < 0 && tots[r] > 0.f) owner = r;
-  const float prefix = pre[owner];
-  int found = INT_MAX;
-  if (owner == rank) {
-    if (prefix + (excl + run) > target || threadIdx.x == kST - 1) {
-      float acc = 0.f;
-      for (int k = s0; k < s1; ++k) {
-        acc += sl.buf[k];
-        if (prefix + (excl + acc) > target) {
-          found = k;
-          break;
-        }
-      }
-    }
-    found = block_min_i(found, sh);
-    if (found == INT_MAX) {
-      // rounding left nothing above target: take the last nonzero entry
-      int last = -1;
-      for (int k = s0; k < s1; ++k)
-        if (sl.buf[k] > 0.f) last = k;
-      const int neg = block_min_i(-last, sh);  // -(largest index)
-      found = (neg <= 0) ? -neg : INT_MAX;
-    }
-  }
-  const Slot o = cluster_from(
-      Slot{(unsigned long long)(unsigned)(found == INT_MAX ? 0 : sl.lo + found), 0ull}, owner, CS,
-      ph, sh);
-  return (int)(unsigned)o.a;
+// the first child of node v after child c (storage order), -1 if none
+SPEC_DEV int next_child(const int* par, int v, int c, int R) {
+  for (int c2 = c + 1; c2 < R; ++c2)
+    if (par[c2] == v) return c2;
+  return -1;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -856,31 +730,66 @@ SPEC_DEV int draw_from_slice(const Slice& sl, float u, int rank, int CS, int& ph
 //   tree node v: the first accepted child (residual p' updated after each
 //     rejected child) or, if none, the final token drawn from p'.
 // The cluster that finishes a sequence's last row assembles the sequence.
-__global__ void __launch_bounds__(kST, 1) sampler_kernel(const SP p) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
+  constexpr int NW = NT / 32;
+  constexpr int kWL = kListPerCTA / NW;
   extern __shared__ __align__(16) uint8_t dyn[];
-  float* Lb = reinterpret_cast<float*>(dyn);
-  float* Eb = Lb + p.slice;
-  Scratch sc;
-  sc.cand = reinterpret_cast<uint64_t*>(Eb + p.slice);
-  sc.gk = sc.cand + kCandMax;
-  sc.sk = sc.gk + kCandMax;
-  sc.candE = reinterpret_cast<float*>(sc.sk + kCandMax);
-  sc.ge = sc.candE + kCandMax;
-  sc.se = sc.ge + kCandMax;
-  __shared__ Shared sh;
-  const int rank = (int)cluster_ctarank();
+  float* buf = reinterpret_cast<float*>(dyn);
+  uint32_t* hcnt = reinterpret_cast<uint32_t*>(dyn + ((size_t)p.slice * 4 + 15) / 16 * 16);
+  uint32_t* hm = hcnt + kHistPad;  // per-bin sums of m16 (this CTA)
+  unsigned long long* mkey = reinterpret_cast<unsigned long long*>(hm + kHistPad);  // local members
+  unsigned long long* gkey = mkey + kCandMax;  // gathered members
+  uint32_t* mbits = reinterpret_cast<uint32_t*>(gkey + kCandMax);
+  uint32_t* gbits = mbits + kCandMax;
+  uint16_t* lists = reinterpret_cast<uint16_t*>(gbits + kCandMax);
+  float* qb = reinterpret_cast<float*>(lists + kListPerCTA);  // q slice (full-vocabulary residuals)
+  // the radix fallback reuses the member arrays (12 KB) as its scratch
+  const RadixScratch rs{reinterpret_cast<uint32_t*>(mkey), mkey + 256, mkey + 768,
+                        reinterpret_cast<uint32_t*>(mkey) + 2048};
+  __shared__ Sh<NW> sh;
+
   const int CS = (int)cluster_nctarank();
-  const int row = blockIdx.y;
+  const int rank = (int)cluster_ctarank();
+  const int row = blockIdx.x / CS;
   const int R = p.R;
   const int b = row / R;
   const int i = row % R;
-  Slice sl{Lb, rank * p.slice, 0};
-  sl.n = max(0, min(p.slice, p.V - sl.lo));
-  Slice sw{Eb, sl.lo, sl.n};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lo = rank * p.slice;
+  const int n = max(0, min(p.slice, p.V - lo));
+  const float* lrow_full = p.logits + (size_t)row * p.V;
+  const float* lrow = lrow_full + lo;
+  const bool topk = p.top_k > 0 && p.top_k < p.V;
+  const bool topp = p.top_p > 0.f && p.top_p < 1.f;
+  const bool trunc = !p.greedy && (topk || topp);
   int ph = 0;
-  uint32_t bar_phase = 0;
 
-  // the q row this row may need for its residual: warm it into L2 now
+  // ---- 0. setup: barrier, histogram, tree shape, this row's probe token
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_mbar_init();
+    sh.token_in = -1;
+  }
+  if (trunc)
+    for (int k = threadIdx.x; k < kHist; k += NT) {
+      hcnt[k] = 0u;
+      hm[k] = 0u;
+    }
+  if (p.tree)
+    for (int c = threadIdx.x; c < R; c += NT) {
+      sh.par[c] = p.parent[(size_t)b * R + c];
+      sh.tok[c] = p.tokens[(size_t)b * R + c];
+    }
+  __syncthreads();
+  // the token whose E this row's first test needs (-1: no test)
+  int probe = -1;
+  if (!p.tree) {
+    if (i < R - 1) probe = __ldg(&p.tokens[(size_t)b * (R - 1) + i]);
+  } else {
+    const int fc = next_child(sh.par, i, i, R);
+    if (fc >= 0) probe = sh.tok[fc];
+  }
   const float* qrow = nullptr;
   if (!p.greedy && p.q) {
     if (p.tree)
@@ -888,189 +797,608 @@ __global__ void __launch_bounds__(kST, 1) sampler_kernel(const SP p) {
     else if (i < R - 1)
       qrow = p.q + ((size_t)b * (R - 1) + i) * p.V;
   }
-  if (threadIdx.x == 0) {
-    mbar_init(&sh.bar, 1);
-    fence_mbar_init();
-    if (qrow && p.qbulk && sl.n > 0) prefetch_l2(qrow + sl.lo, (uint32_t)sl.n * 4u);
-  }
-  if (p.tree)
-    for (int c = threadIdx.x; c < R; c += kST) {
-      sh.par[c] = p.parent[(size_t)b * R + c];
-      sh.tok[c] = p.tokens[(size_t)b * R + c];
-    }
-  // scalars of this row's test, loaded early
-  float u_test = 0.f, u_final = 0.f;
-  int x_draft = -1;
-  if (!p.greedy) {
-    u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
-    if (!p.tree && i < R - 1) {
-      u_test = __ldg(&p.u[(size_t)b * R + i]);
-      x_draft = __ldg(&p.tokens[(size_t)b * (R - 1) + i]);
-    }
-  }
-  __syncthreads();
+  // full-vocabulary residuals read q from shared memory (loaded with the logits)
+  const bool q_sh = p.qsm && qrow != nullptr && n > 0;
 
-  // ---- 1. the row into shared memory
-  load_row(p, p.logits + (size_t)row * p.V, sl, sh, bar_phase);
-
-  // ---- 2. max, lowest-id argmax, non-finite check
-  float mv = -INFINITY;
-  int mi = INT_MAX;
-  int bad = 0;
-  for (int k = threadIdx.x; k < sl.n; k += kST) {
-    const float x = sl.buf[k];
-    if (isnan(x) || x == INFINITY) bad = 1;
-    if (x > mv || (x == mv && sl.lo + k < mi)) {
-      mv = x;
-      mi = sl.lo + k;
-    }
-  }
-  bad = block_or(bad, sh);
-  block_max_arg(mv, mi, sh);
-  cluster_allgather(Slot{((unsigned long long)__float_as_uint(mv) << 32) | (unsigned)mi,
-                         (unsigned long long)bad},
-                    CS, ph, sh);
-  for (int r = 0; r < CS; ++r) {
-    const unsigned long long a = sh.gath[r].a;
-    const float ov = __uint_as_float((uint32_t)(a >> 32));
-    const int oi = (int)(uint32_t)a;
-    bad |= (int)sh.gath[r].b;
-    if (ov > mv || (ov == mv && oi < mi)) {
-      mv = ov;
-      mi = oi;
-    }
-  }
-  if (mv == -INFINITY) bad = 1;  // every token banned: no distribution
-  const float m = mv;
-  Outcome oc{0, -1, 0, bad};
-
-  if (p.greedy) {
-    // ---- greedy: the argmax decides everything
-    if (!bad) {
-      if (!p.tree) {
-        if (i < R - 1) oc.accept = (__ldg(&p.tokens[(size_t)b * (R - 1) + i]) == mi) ? 1 : 0;
-        oc.token = mi;
-      } else {
-        oc.accept = -1;
-        for (int c = i + 1; c < R; ++c)
-          if (sh.par[c] == i && sh.tok[c] == mi) {
-            oc.accept = c;
-            break;
-          }
-        oc.token = mi;
+  // ---- 1. the slice (and q's) into shared memory
+  if (n > 0) {
+    if (p.bulk) {
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&sh.bar, (uint32_t)n * (q_sh ? 8u : 4u));
+        bulk_load(buf, lrow, (uint32_t)n * 4u, &sh.bar);
+        if (q_sh) bulk_load(qb, qrow + lo, (uint32_t)n * 4u, &sh.bar);
       }
-    }
-  } else if (!bad) {
-    // ---- 3. exp values, normaliser, truncation
-    Kahan acc;
-    for (int k = threadIdx.x; k < sl.n; k += kST) {
-      const float e = texp(sl.buf[k], m, p.T, p.invT);
-      Eb[k] = e;
-      acc.add(e);
-    }
-    const DF zall = cluster_sum_df(block_sum_df(acc.df(), sh), CS, ph, sh);
-    Trunc tr{0u, INT_MAX, zall, true};
-    if ((p.top_k > 0 && p.top_k < p.V) || (p.top_p > 0.f && p.top_p < 1.f)) {
-      tr = truncate_fast(p, sl, Eb, sc, m, zall, rank, CS, ph, sh);
-      if (!tr.ok) {
-        tr = truncate_radix(p, sl, m, rank, CS, ph, sh);
-        const uint32_t tau = tr.tau;
-        const int tie = tr.tie;
-        tr.Z = cluster_masked_sum(
-            sl, Eb, [&](int k) { return is_kept(okey(sl.buf[k]), sl.lo + k, tau, tie); }, CS,
-            ph, sh);
-      }
-    }
-    const float invZ = 1.0f / (float)df_d(tr.Z);
-    const bool truncated = tr.tau != 0u || tr.tie != INT_MAX;
-    // p in place of the exp values (0 outside the kept set)
-    if (truncated) {
-      for (int k = threadIdx.x; k < sl.n; k += kST)
-        Eb[k] = is_kept(okey(sl.buf[k]), sl.lo + k, tr.tau, tr.tie) ? Eb[k] * invZ : 0.f;
+      mbar_wait(&sh.bar, 0, p.err);
     } else {
-      for (int k = threadIdx.x; k < sl.n; k += kST) Eb[k] *= invZ;
+      for (int k = threadIdx.x; k < n; k += NT) buf[k] = __ldg(lrow + k);
+      __syncthreads();
+    }
+  }
+
+  // ---- 2. maximum (NaN-propagating), greedy argmax
+  float mx = -INFINITY, best = -INFINITY;
+  int bid = INT_MAX;
+  {
+    const int n4 = n >> 2;
+    const float4* b4 = reinterpret_cast<const float4*>(buf);
+    for (int k4 = threadIdx.x; k4 < n4; k4 += NT) {
+      const float4 v = b4[k4];
+      mx = fmax_nan(fmax_nan(mx, v.x), fmax_nan(fmax_nan(v.y, v.z), v.w));
+      if (p.greedy) {
+        if (v.x > best) { best = v.x; bid = 4 * k4; }
+        if (v.y > best) { best = v.y; bid = 4 * k4 + 1; }
+        if (v.z > best) { best = v.z; bid = 4 * k4 + 2; }
+        if (v.w > best) { best = v.w; bid = 4 * k4 + 3; }
+      }
+    }
+    for (int k = 4 * n4 + threadIdx.x; k < n; k += NT) {
+      const float v = buf[k];
+      mx = fmax_nan(mx, v);
+      if (p.greedy && v > best) { best = v; bid = k; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
+      const float ob = __shfl_xor_sync(kFull, best, o);
+      const int oi = __shfl_xor_sync(kFull, bid, o);
+      if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
+    }
+    if (lane == 0) { sh.red_f[warp] = mx; sh.wsum[warp] = best; sh.red_i[warp] = bid; }
+    __syncthreads();
+    mx = sh.red_f[0]; best = sh.wsum[0]; bid = sh.red_i[0];
+    for (int w = 1; w < NW; ++w) {
+      mx = fmax_nan(mx, sh.red_f[w]);
+      if (sh.wsum[w] > best || (sh.wsum[w] == best && sh.red_i[w] < bid)) {
+        best = sh.wsum[w]; bid = sh.red_i[w];
+      }
     }
     __syncthreads();
-    if (p.p_out) {
-      float* dst = p.p_out + (size_t)row * p.V + sl.lo;
-      for (int k = threadIdx.x; k < sl.n; k += kST) dst[k] = Eb[k];
+  }
+  exchange(Post{{f2w(mx), f2w(best),
+                 (unsigned long long)(unsigned)(bid == INT_MAX ? INT_MAX : lo + bid), 0ull}},
+           CS, ph, sh);
+  float m = -INFINITY;
+  int argmax = INT_MAX;
+  best = -INFINITY;
+  for (int r = 0; r < CS; ++r) {
+    m = fmax_nan(m, w2f(sh.gath[r].w[0]));
+    const float ob = w2f(sh.gath[r].w[1]);
+    const int oi = (int)(unsigned)sh.gath[r].w[2];
+    if (ob > best || (ob == best && oi < argmax)) { best = ob; argmax = oi; }
+  }
+  const bool bad = isnan(m) || m == INFINITY || m == -INFINITY;
+  Outcome oc{0, -1, 0, bad ? 1 : 0};
+  bool drew = false;    // this row made a draw (same in every CTA of the cluster)
+  int draw_token = -1;  // set by the draw's owner CTA only
+
+  if (bad) {
+    // no distribution: the sequence reports NONFINITE
+  } else if (p.greedy) {
+    if (!p.tree) {
+      if (i < R - 1) oc.accept = (probe == argmax) ? 1 : 0;
+    } else {
+      oc.accept = -1;
+      for (int c = i + 1; c < R; ++c)
+        if (sh.par[c] == i && sh.tok[c] == argmax) { oc.accept = c; break; }
+    }
+    oc.token = argmax;
+  } else {
+    // ---- 3. E in place, Z (compensated per thread), histogram, probe value
+    const float nm = -m, lfloor = m - 150.f * p.T;
+    const float c_hi = p.c_hi, c_lo = p.c_lo;
+    float zs = 0.f, zc = 0.f;  // Kahan sum and compensation
+    {
+      const int n4 = n >> 2;
+      float4* b4 = reinterpret_cast<float4*>(buf);
+      for (int k4 = threadIdx.x; k4 < n4; k4 += NT) {
+        const float4 v = b4[k4];
+        float4 e;
+        e.x = texp(v.x, nm, lfloor, c_hi, c_lo);
+        e.y = texp(v.y, nm, lfloor, c_hi, c_lo);
+        e.z = texp(v.z, nm, lfloor, c_hi, c_lo);
+        e.w = texp(v.w, nm, lfloor, c_hi, c_lo);
+        b4[k4] = e;
+        const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float y = ev[j] - zc;
+          const float t = zs + y;
+          zc = (t - zs) - y;
+          zs = t;
+          if (trunc) {
+            const uint32_t bits = __float_as_uint(ev[j]);
+            const int bn = ebin(bits);
+            if (topk) atomicAdd(&hcnt[bn], 1u);
+            if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+          }
+        }
+      }
+      for (int k = 4 * n4 + threadIdx.x; k < n; k += NT) {
+        const float e = texp(buf[k], nm, lfloor, c_hi, c_lo);
+        buf[k] = e;
+        const float y = e - zc;
+        const float t = zs + y;
+        zc = (t - zs) - y;
+        zs = t;
+        if (trunc) {
+          const uint32_t bits = __float_as_uint(e);
+          const int bn = ebin(bits);
+          if (topk) atomicAdd(&hcnt[bn], 1u);
+          if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+        }
+      }
+    }
+    const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: buf and histogram complete
+    const float zl = block_sum_f<NT>(-zc, sh);
+    if (trunc && warp == 0) {  // per-octave totals of this CTA's bins
+      uint32_t c = 0, mm = 0;
+      for (int j = 0; j < 32; ++j) {
+        c += hcnt[32 * lane + j];
+        mm += hm[32 * lane + j];
+      }
+      sh.oct[lane] = c;
+      sh.oct[32 + lane] = mm;
+    }
+    const bool pin = probe >= lo && probe < lo + n;
+    exchange(Post{{f2w(zh), f2w(zl), f2w(pin ? buf[probe - lo] : 0.f), 0ull}}, CS, ph, sh);
+    float e_probe = 0.f;
+    if (probe >= 0 && probe < p.V) e_probe = w2f(sh.gath[probe / p.slice].w[2]);
+    float zah = 0.f, zal = 0.f;  // Z of the whole row, float pair
+    for (int r = 0; r < CS; ++r) df_acc(zah, zal, w2f(sh.gath[r].w[0]), w2f(sh.gath[r].w[1]));
+
+    Cut cut{0, 0.f, 0u, INT_MAX};
+    float zkept = zah + zal;
+    int tmode = 0;
+    if (trunc) {
+      // ---- 4. the bin range the cut can fall in (warp 0): octave totals of
+      // the cluster (lane = octave), then the bins of the octaves the
+      // crossings fall in (lane = bin within the octave)
+      if (warp == 0) {
+        unsigned long long oc_c = 0, oc_m = 0;
+        for (int r = 0; r < CS; ++r) {
+          if (topk) oc_c += dsmem_ld_u32(&sh.oct[lane], r);
+          if (topp) oc_m += dsmem_ld_u32(&sh.oct[32 + lane], r);
+        }
+        oc_m = bin_fx(oc_m, 32 * lane);  // all bins of an octave share one exponent
+        unsigned long long xc = oc_c, xm = oc_m;  // inclusive scans over octaves
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long tc = __shfl_up_sync(kFull, xc, o);
+          const unsigned long long tmv = __shfl_up_sync(kFull, xm, o);
+          if (lane >= o) { xc += tc; xm += tmv; }
+        }
+        const unsigned long long pc = xc - oc_c, pm = xm - oc_m;  // before each octave
+        // cluster totals of the bins of octave o (lane j: bin 32 o + j)
+        auto load_oct = [&](int o, unsigned long long& bc, unsigned long long& bmass) {
+          bc = 0;
+          unsigned long long mm = 0;
+          for (int r = 0; r < CS; ++r) {
+            if (topk) bc += dsmem_ld_u32(&hcnt[32 * o + lane], r);
+            if (topp) mm += dsmem_ld_u32(&hm[32 * o + lane], r);
+          }
+          bmass = bin_fx(mm, 32 * o);
+        };
+        // inclusive scan over the lanes
+        auto scan = [&](unsigned long long v) {
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += t;
+          }
+          return v;
+        };
+        // first lane where po + running value reaches thr (31 if none)
+        auto first_at = [&](unsigned long long po, unsigned long long incl,
+                            unsigned long long thr) -> int {
+          const unsigned h = __ballot_sync(kFull, po + incl >= thr);
+          return h ? __ffs(h) - 1 : 31;
+        };
+        int mode = 1, b_lo = 0, b_hi = 0, kidx = -1, members = -1;
+        if (topk) {
+          const unsigned h = __ballot_sync(kFull, xc >= (unsigned long long)p.top_k);
+          if (!h) {
+            mode = 2;  // the k-th largest lies below 2^-32 of the maximum
+          } else {
+            const int ok = __ffs(h) - 1;
+            unsigned long long bc, bmass;
+            load_oct(ok, bc, bmass);
+            const unsigned long long ic = scan(bc);
+            const unsigned long long pck = __shfl_sync(kFull, pc, ok);
+            const int jk = first_at(pck, ic, (unsigned long long)p.top_k);
+            const int bk = 32 * ok + jk;
+            b_lo = b_hi = bk;
+            const int cnt_before_bk = (int)(pck + __shfl_sync(kFull, ic - bc, jk));
+            kidx = p.top_k - cnt_before_bk - 1;
+            members = (int)__shfl_sync(kFull, bc, jk);
+            if (topp) {
+              // the mass above bk, then the bin where top_p times it is reached
+              const unsigned long long im = scan(bmass);
+              const unsigned long long abk =
+                  __shfl_sync(kFull, pm, ok) + __shfl_sync(kFull, im - bmass, jk);
+              const unsigned long long thr = (unsigned long long)((double)p.top_p * (double)abk);
+              const unsigned h2 = __ballot_sync(kFull, xm >= thr);
+              int ol = h2 ? __ffs(h2) - 1 : ok;
+              if (ol > ok) ol = ok;
+              unsigned long long lc = bc, lm = bmass, ilc = ic, ilm = im;
+              if (ol != ok) {
+                load_oct(ol, lc, lm);
+                ilc = scan(lc);
+                ilm = scan(lm);
+              }
+              int bl = 32 * ol + first_at(__shfl_sync(kFull, pm, ol), ilm, thr);
+              if (bl > bk) bl = bk;
+              b_lo = bl;
+              // members in [b_lo, bk], and the count above b_lo
+              const int jl = bl - 32 * ol;
+              unsigned long long inrange;
+              if (ol == ok) {
+                inrange = (lane >= jl && lane <= jk) ? bc : 0;
+              } else {
+                inrange = (lane >= jl ? lc : 0) + (lane <= jk ? bc : 0) +
+                          ((lane > ol && lane < ok) ? oc_c : 0);
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) inrange += __shfl_xor_sync(kFull, inrange, o);
+              members = (int)inrange;
+              const int cnt_before_bl =
+                  (int)(__shfl_sync(kFull, pc, ol) + __shfl_sync(kFull, ilc - lc, jl));
+              kidx = p.top_k - cnt_before_bl - 1;
+            }
+          }
+        } else {
+          const double zd = (double)zah + (double)zal;
+          const unsigned long long thr = (unsigned long long)((double)p.top_p * zd * kFx);
+          const unsigned h = __ballot_sync(kFull, xm >= thr);
+          if (!h) {
+            mode = 2;
+          } else {
+            const int ol = __ffs(h) - 1;
+            unsigned long long bc, bmass;
+            load_oct(ol, bc, bmass);
+            const int jl = first_at(__shfl_sync(kFull, pm, ol), scan(bmass), thr);
+            b_lo = b_hi = 32 * ol + jl;
+          }
+        }
+        if (mode == 1 && members > NT) mode = 2;  // the selection sorts at most NT members
+        if (lane == 0) {
+          sh.bi[0] = mode;
+          sh.bi[1] = b_lo;
+          sh.bi[2] = b_hi;
+          sh.bi[3] = kidx;
+        }
+      }
+      __syncthreads();
+      tmode = sh.bi[0];
+      const int b_lo = sh.bi[1], b_hi = sh.bi[2], kidx = sh.bi[3];
+      __syncthreads();
+
+      if (tmode == 1) {
+        // ---- 5. members of bins [b_lo, b_hi] and the exact mass above them
+        if (threadIdx.x == 0) sh.bi[4] = 0;
+        __syncthreads();
+        unsigned long long above = 0;
+        // E in bins <= b_hi  <=>  bits >= edge (bins count down from E = 1)
+        const uint32_t edge = (uint32_t)(0x3F7FFFFF - ((b_hi + 1) << 18) + 1);
+        auto visit = [&](int k, float e) {
+          const uint32_t bits = __float_as_uint(e);
+          if (bits < edge) return;
+          const int bn = ebin(bits);
+          if (bn < b_lo) {
+            above += fx44(bits);
+          } else if (bn <= b_hi) {
+            const int slot = atomicAdd(&sh.bi[4], 1);
+            if (slot < kCandMax) {
+              mkey[slot] = ((unsigned long long)okey(__ldg(lrow + k)) << 32) |
+                           (0xFFFFFFFFu - (uint32_t)(lo + k));
+              mbits[slot] = bits;
+            }
+          }
+        };
+        {
+          const int n4 = n >> 2;
+          const float4* b4 = reinterpret_cast<const float4*>(buf);
+          for (int k4 = threadIdx.x; k4 < n4; k4 += NT) {
+            const float4 e = b4[k4];
+            visit(4 * k4, e.x);
+            visit(4 * k4 + 1, e.y);
+            visit(4 * k4 + 2, e.z);
+            visit(4 * k4 + 3, e.w);
+          }
+          for (int k = 4 * n4 + threadIdx.x; k < n; k += NT) visit(k, buf[k]);
+        }
+        above = block_sum_u64<NT>(above, sh);  // includes barriers: members complete
+        exchange(Post{{(unsigned long long)sh.bi[4], above, 0ull, 0ull}}, CS, ph, sh);
+        unsigned long long a_lo = 0;
+        int total = 0;
+        for (int r = 0; r < CS; ++r) {
+          a_lo += sh.gath[r].w[1];
+          total += (int)sh.gath[r].w[0];
+        }
+        if (total > NT || total < 1) {
+          tmode = 2;  // too populous to sort here (top-p only: counted now)
+        } else {
+          // gather into registers: thread t holds member t
+          const int t = threadIdx.x;
+          unsigned long long key = 0ull;
+          uint32_t eb = 0u;
+          {
+            int off = 0;
+            for (int r = 0; r < CS; ++r) {
+              const int cr = (int)sh.gath[r].w[0];
+              if (t >= off && t < off + cr) {
+                key = dsmem_ld_u64(&mkey[t - off], r);
+                eb = dsmem_ld_u32(&mbits[t - off], r);
+              }
+              off += cr;
+            }
+          }
+          int P = 1;
+          while (P < total) P <<= 1;
+          // bitonic sort, descending key (= logit desc, id asc): shuffles within
+          // a warp, shared memory across warps
+          for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+              unsigned long long ok2;
+              uint32_t ob;
+              if (stride >= 32) {
+                if (t < P) {
+                  gkey[t] = key;
+                  gbits[t] = eb;
+                }
+                __syncthreads();
+                ok2 = (t < P) ? gkey[t ^ stride] : 0ull;
+                ob = (t < P) ? gbits[t ^ stride] : 0u;
+                __syncthreads();
+              } else {
+                ok2 = __shfl_xor_sync(kFull, key, stride);
+                ob = __shfl_xor_sync(kFull, eb, stride);
+              }
+              const bool desc = (t & size) == 0;
+              const bool lower = (t & stride) == 0;
+              const bool take = lower ? (desc ? ok2 > key : ok2 < key) : (desc ? ok2 < key : ok2 > key);
+              if (take) {
+                key = ok2;
+                eb = ob;
+              }
+            }
+          }
+          // ---- 5b. the cut on exact masses: thread t holds the t-th largest member
+          const bool live = t < total;
+          const unsigned long long mt = live ? fx44(eb) : 0ull;
+          const unsigned long long incl = a_lo + block_incl_scan_u64<NT>(mt, sh);  // mass through t
+          const int last = (kidx >= 0) ? min(kidx, total - 1) : total - 1;
+          if (threadIdx.x == 0) {
+            sh.bi[5] = 0;
+            if (kidx < 0) sh.zk = (unsigned long long)(((double)zah + (double)zal) * kFx);
+          }
+          __syncthreads();
+          if (kidx >= 0 && t == last) sh.zk = incl;  // Z after top-k
+          __syncthreads();
+          const unsigned long long zk = sh.zk;
+          int pick = -1;
+          if (!topp) {
+            if (t == last) pick = t;
+          } else {
+            const unsigned long long thr = (unsigned long long)((double)p.top_p * (double)zk);
+            if (live && t <= last && incl - mt < thr && incl >= thr) pick = t;
+          }
+          if (pick >= 0) {  // unique: masses are positive
+            sh.cut = Cut{1, __uint_as_float(eb), (uint32_t)(key >> 32),
+                         (int)(0xFFFFFFFFu - (uint32_t)key)};
+            sh.zcut = incl;
+            sh.bi[5] = 1;
+          }
+          __syncthreads();
+          if (sh.bi[5]) {
+            cut = sh.cut;
+            zkept = (float)sh.zcut * (1.0f / 17592186044416.0f);  // 2^-44
+          } else {
+            tmode = 2;  // the rounded bin masses placed the cut one bin off
+          }
+          __syncthreads();
+        }
+      }
+      if (tmode == 2) {
+        // ---- 5'. exact radix selection over the logit keys
+        cluster_sync();  // every CTA is done reading the others' member lists
+        cut = cut_radix<NT>(p, lrow, buf, n, lo, rs, rank, CS, ph, sh);
+        // Z over the kept set (compensated per thread, fixed order)
+        float s = 0.f, cmp = 0.f;
+        for (int k = threadIdx.x; k < n; k += NT) {
+          if (cut_keeps(cut, buf[k], lo + k, lrow_full)) {
+            const float y = buf[k] - cmp;
+            const float tt = s + y;
+            cmp = (tt - s) - y;
+            s = tt;
+          }
+        }
+        const float hs = block_sum_f<NT>(s, sh);
+        const float ls = block_sum_f<NT>(-cmp, sh);
+        exchange(Post{{f2w(hs), f2w(ls), 0ull, 0ull}}, CS, ph, sh);
+        float kh = 0.f, kl = 0.f;
+        for (int r = 0; r < CS; ++r) df_acc(kh, kl, w2f(sh.gath[r].w[0]), w2f(sh.gath[r].w[1]));
+        zkept = kh + kl;
+      }
     }
 
+    // ---- 6. (tree, p_out: on first use) zero the cut-off tail in place and
+    // list each warp's kept positions
+    const int rw = ((n + NW - 1) / NW + 3) / 4 * 4;
+    Items<NW> it{false, lists, min(warp * rw, n), min((warp + 1) * rw, n)};
+    bool kept_ready = !trunc, zeroed = !trunc;
+    // zero: also clear buf outside the kept set (needed where buf is read by
+    // position: the tree's probe values and p_out)
+    auto ensure_kept = [&](bool zero) {
+      if (kept_ready && (zeroed || !zero)) return;
+      kept_ready = true;
+      zeroed = zeroed || zero;
+      int cntw = 0;
+      uint16_t* myl = lists + warp * kWL;
+      const int r1v = it.r0 + ((it.r1 - it.r0) & ~3);
+      for (int s0 = it.r0; s0 < it.r1; s0 += 128) {
+        const int k = s0 + 4 * lane;
+        int c = 0;
+        bool kp[4] = {false, false, false, false};
+        if (k < r1v) {
+          float4 e4 = *reinterpret_cast<const float4*>(buf + k);
+          float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            kp[u] = ev[u] > 0.f && cut_keeps(cut, ev[u], lo + k + u, lrow_full);
+            if (!kp[u]) ev[u] = 0.f;
+            c += kp[u] ? 1 : 0;
+          }
+          if (zero) *reinterpret_cast<float4*>(buf + k) = make_float4(ev[0], ev[1], ev[2], ev[3]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (k + u < it.r1) {
+              const float e = buf[k + u];
+              kp[u] = e > 0.f && cut_keeps(cut, e, lo + k + u, lrow_full);
+              if (!kp[u] && zero) buf[k + u] = 0.f;
+              c += kp[u] ? 1 : 0;
+            }
+          }
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int tt = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += tt;
+        }
+        int pos = cntw + incl - c;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (kp[u]) {
+            if (pos < kWL) myl[pos] = (uint16_t)(k + u);
+            ++pos;
+          }
+        cntw += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) sh.list_n[warp] = cntw;
+      it.listed = __syncthreads_and(cntw <= kWL ? 1 : 0) != 0;
+    };
+    const float invz = 1.0f / zkept;
+    if (p.p_out) {
+      ensure_kept(true);
+      float* dst = p.p_out + (size_t)row * p.V + lo;
+      for (int k = threadIdx.x; k < n; k += NT) dst[k] = buf[k] * invz;
+    }
+
+    const float u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    const float* qlo = q_sh ? qb : (qrow ? qrow + lo : nullptr);
     if (!p.tree) {
-      // ---- 4a. chain: this row's test, then its correction or bonus draw
-      bool draw = true;
+      // ---- 7a. chain: the row's test, then its correction or bonus draw
       bool resid = false;
       if (i < R - 1) {
-        const int x = x_draft;
+        const int x = probe;
         const bool xin = x >= 0 && x < p.V;
         const float qx = xin ? __ldg(&qrow[x]) : 0.f;
-        cluster_sync();  // p complete in every CTA
-        const float px =
-            xin ? dsmem_ld_f32(&Eb[x - (x / p.slice) * p.slice], (uint32_t)(x / p.slice)) : 0.f;
+        const float px = (xin && e_probe > 0.f && cut_keeps(cut, e_probe, x, lrow_full))
+                             ? e_probe * invz : 0.f;
         if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
-        oc.accept = (u_test * qx < px) ? 1 : 0;
-        cluster_sync();  // nobody rewrites p before every CTA has read p(x)
-        draw = !oc.accept;
-        resid = true;
+        oc.accept = (__ldg(&p.u[(size_t)b * R + i]) * qx < px) ? 1 : 0;
+        resid = !oc.accept;
       }
-      if (draw) {
-        if (resid) {
-          for (int k = threadIdx.x; k < sl.n; k += kST)
-            Eb[k] = fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f);
-          __syncthreads();
-        }
-        int tok = draw_from_slice(sw, u_final, rank, CS, ph, sh);
-        if (tok == -2) {  // residual with zero mass (rounding only): draw from p
+      drew = i == R - 1 || resid;
+      if (drew) {
+        // truncated: the kept positions listed per warp (buf left as is);
+        // otherwise (or when a list overflows) the whole warp range with the
+        // cut applied inline
+        ensure_kept(false);
+        float t;
+        if (it.listed)
+          t = weight_pass<NT>(buf, it, resid ? 1 : 0, invz, qlo, q_sh, sh);
+        else
+          t = weight_full<NT>(buf, it.r0, it.r1, cut, lo, lrow_full, resid ? 1 : 0, invz, qlo,
+                              q_sh, p.qbulk != 0, sh);
+        exchange(Post{{f2w(t), 0ull, 0ull, 0ull}}, CS, ph, sh);
+        int tokn = locate<NT>(buf, it, lo, u_final, rank, CS, sh);
+        if (tokn == -2) {  // residual with zero mass (rounding only): draw from p
           oc.status |= SPEC_SEQ_RESID_ZERO;
-          for (int k = threadIdx.x; k < sl.n; k += kST)
-            Eb[k] = is_kept(okey(sl.buf[k]), sl.lo + k, tr.tau, tr.tie)
-                        ? texp(sl.buf[k], m, p.T, p.invT) * invZ
-                        : 0.f;
+          for (int k = it.r0 + lane; k < it.r1; k += 32)
+            buf[k] = texp(__ldg(lrow + k), nm, lfloor, c_hi, c_lo);
           __syncthreads();
-          tok = draw_from_slice(sw, u_final, rank, CS, ph, sh);
+          it.listed = false;
+          const float t2 = weight_full<NT>(buf, it.r0, it.r1, cut, lo, lrow_full, 0, 1.f, qlo,
+                                           q_sh, false, sh);
+          exchange(Post{{f2w(t2), 0ull, 0ull, 0ull}}, CS, ph, sh);
+          tokn = locate<NT>(buf, it, lo, u_final, rank, CS, sh);
         }
-        oc.token = tok;
+        draw_token = tokn;
       }
     } else {
-      // ---- 4b. tree node: children in storage order against the running p'
+      // ---- 7b. tree node: children in storage order against the running p'
       oc.accept = -1;
-      for (int c = i + 1; c < R; ++c) {
-        if (sh.par[c] != i) continue;
+      float invw = invz;
+      int nsteps = 0;
+      float v_probe = (e_probe > 0.f && probe >= 0 && probe < p.V &&
+                       cut_keeps(cut, e_probe, probe, lrow_full)) ? e_probe : 0.f;
+      for (int c = next_child(sh.par, i, i, R); c >= 0; c = next_child(sh.par, i, c, R)) {
         const int t = sh.tok[c];
         const bool tin = t >= 0 && t < p.V;
-        const float qx = tin ? __ldg(&qrow[t]) : 0.f;
-        cluster_sync();  // p' complete everywhere
-        const float pt =
-            tin ? dsmem_ld_f32(&Eb[t - (t / p.slice) * p.slice], (uint32_t)(t / p.slice)) : 0.f;
-        cluster_sync();  // nobody rewrites p' before every CTA has read it
-        if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
-        if (__ldg(&p.u[(size_t)b * R + (c - 1)]) * qx < pt) {
+        const float qt = tin ? __ldg(&qrow[t]) : 0.f;
+        const float pt = tin ? v_probe * invw : 0.f;
+        if (qt == 0.f) oc.status |= SPEC_SEQ_QZERO;
+        if (__ldg(&p.u[(size_t)b * R + (c - 1)]) * qt < pt) {
           oc.accept = c;
           break;
         }
+        // the next child's token: the exchange carries its p' value
+        const int nc = next_child(sh.par, i, c, R);
+        const int tn = nc >= 0 ? sh.tok[nc] : -1;
+        const bool tnin = tn >= lo && tn < lo + n;
         // p' <- norm(max(0, p' - q_v))
-        Kahan w;
-        for (int k = threadIdx.x; k < sl.n; k += kST)
-          w.add(fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f));
-        const DF W = cluster_sum_df(block_sum_df(w.df(), sh), CS, ph, sh);
-        const float Wf = (float)df_d(W);
-        if (Wf > 0.f) {
-          const float invW = 1.0f / Wf;
-          for (int k = threadIdx.x; k < sl.n; k += kST)
-            Eb[k] = fmaxf(Eb[k] - __ldg(&qrow[sl.lo + k]), 0.f) * invW;
+        ensure_kept(true);
+        if (threadIdx.x == 0) sh.invw_used[nsteps] = invw;
+        const float wt = weight_pass<NT>(buf, it, 1, invw, qlo, q_sh, sh);
+        exchange(Post{{f2w(wt), f2w(tnin ? buf[tn - lo] : 0.f), 0ull, 0ull}}, CS, ph, sh);
+        float W = 0.f;
+        for (int r = 0; r < CS; ++r) W += w2f(sh.gath[r].w[0]);
+        const float vn = (tn >= 0 && tn < p.V) ? w2f(sh.gath[tn / p.slice].w[1]) : 0.f;
+        if (W > 1e-37f) {
+          invw = 1.0f / W;
+          ++nsteps;
+          v_probe = vn;
         } else {
+          // zero mass (rounding only): keep p' -- rebuild it from the logits
           oc.status |= SPEC_SEQ_RESID_ZERO;
+          const int cnt = it.count(sh);
+          for (int j = lane; j < cnt; j += 32) {
+            const int k = it.at(j);
+            float e = texp(__ldg(lrow + k), nm, lfloor, c_hi, c_lo);
+            e = cut_keeps(cut, e, lo + k, lrow_full) ? e : 0.f;
+            for (int s = 0; s < nsteps; ++s)
+              e = residual_w(e, sh.invw_used[s],
+                             e > 0.f ? (q_sh ? qlo[k] : __ldg(qlo + k)) : 0.f);
+            buf[k] = e;
+          }
+          __syncthreads();
+          exchange(Post{{0ull, f2w(tnin ? buf[tn - lo] : 0.f), 0ull, 0ull}}, CS, ph, sh);
+          v_probe = (tn >= 0 && tn < p.V) ? w2f(sh.gath[tn / p.slice].w[1]) : 0.f;
         }
-        __syncthreads();
       }
-      if (oc.accept < 0) oc.token = draw_from_slice(sw, u_final, rank, CS, ph, sh);
+      drew = oc.accept < 0;
+      if (drew) {
+        ensure_kept(true);
+        const float t = weight_pass<NT>(buf, it, 0, 1.f, qlo, q_sh, sh);
+        exchange(Post{{f2w(t), 0ull, 0ull, 0ull}}, CS, ph, sh);
+        draw_token = locate<NT>(buf, it, lo, u_final, rank, CS, sh);
+        if (draw_token == -2) oc.status |= SPEC_SEQ_RESID_ZERO;
+      }
     }
   }
 
-  // ---- 5. publish the outcome; the last row of the sequence assembles it
-  cluster_sync();  // every CTA is done with the others' shared memory
+  // ---- 8. the draw's owner hands its token to rank 0; then rank 0 publishes
+  if (draw_token >= 0 && threadIdx.x == 0) {
+    if (rank == 0)
+      sh.token_in = draw_token;
+    else
+      dsmem_st_s32(&sh.token_in, 0, draw_token);
+  }
+  cluster_sync();  // also: no CTA leaves while another may read its shared memory
   if (rank != 0 || threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
+  if (drew) oc.token = sh.token_in;
   int last = 0;
   if (lane == 0) {
     p.outcomes[row] = oc;
@@ -1137,20 +1465,42 @@ __global__ void __launch_bounds__(kST, 1) sampler_kernel(const SP p) {
 
 // ---------------------------------------------------------------- host side
 struct SampPlan {
-  int CS, slice;
-  size_t smem;  // bytes of one slice buffer
+  int CS, slice, NT;
+  size_t smem;  // dynamic shared memory bytes
 };
 
-SampPlan plan_sampler(int V) {
-  SampPlan pl;
-  pl.CS = std::min(kMaxCS, std::max(1, (V + 16383) / 16384));
-  pl.slice = ((V + pl.CS - 1) / pl.CS + 3) / 4 * 4;
-  pl.smem = (size_t)pl.slice * 4;
-  return pl;
+size_t dyn_smem(size_t slice_bytes, bool qsm) {
+  const size_t sb = (slice_bytes + 15) / 16 * 16;
+  return sb + 2 * (size_t)kHistPad * 4 + 2 * (size_t)kCandMax * 12 + (size_t)kListPerCTA * 2 +
+         (qsm ? sb : 0);
 }
 
-size_t dyn_smem(size_t slice_bytes) {
-  return 2 * slice_bytes + 3 * (size_t)kCandMax * (sizeof(uint64_t) + sizeof(float));
+int num_sms_cached() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 152;
+  }
+  return n;
+}
+
+int cluster_size(int V) { return std::min(kMaxCS, std::max(1, (V + 16383) / 16384)); }
+
+int slice_of(int V, int CS) { return ((V + CS - 1) / CS + 3) / 4 * 4; }
+
+SampPlan plan_sampler(int B, int R, int V, bool qsm) {
+  SampPlan pl;
+  pl.CS = cluster_size(V);
+  pl.slice = slice_of(V, pl.CS);
+  // few rows: one 512-thread CTA per SM; many rows: two 256-thread CTAs per SM
+  const long long ctas = (long long)B * R * pl.CS;
+  pl.NT = ctas <= num_sms_cached() ? 512 : 256;
+  pl.smem = dyn_smem((size_t)pl.slice * 4, qsm);
+  return pl;
 }
 
 size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
@@ -1162,21 +1512,19 @@ size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
   return off;
 }
 
-spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
-  const SampPlan pl = plan_sampler(V);
-  prm.slice = pl.slice;
-  if (pl.smem > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
+template <int NT>
+spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t st) {
   static bool attr_set = false;  // once, at the largest size, so graph captures need no setup
   if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dyn_smem(kMaxSliceBytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(sampler_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn_smem(kMaxSliceBytes, true)) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.CS, B * R, 1);
-  cfg.blockDim = dim3(kST, 1, 1);
-  cfg.dynamicSmemBytes = dyn_smem(pl.smem);
+  cfg.gridDim = dim3((unsigned)(pl.CS * rows), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1185,8 +1533,18 @@ spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sampler_kernel, prm) != cudaSuccess) return SPEC_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sampler_kernel<NT>, prm) != cudaSuccess) return SPEC_ECUDA;
   return launch_status();
+}
+
+spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
+  // full-vocabulary residuals (no truncation) stage q's slice in shared memory
+  const bool trunc = (prm.top_k > 0 && prm.top_k < V) || (prm.top_p > 0.f && prm.top_p < 1.f);
+  prm.qsm = (!prm.greedy && prm.qbulk && !trunc) ? 1 : 0;
+  const SampPlan pl = plan_sampler(B, R, V, prm.qsm != 0);
+  if ((size_t)pl.slice * 4 > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
+  prm.slice = pl.slice;
+  return pl.NT == 512 ? launch_nt<512>(prm, pl, B * R, st) : launch_nt<256>(prm, pl, B * R, st);
 }
 
 spec_status check_cfg(const spec_sampler* cfg) {
@@ -1206,7 +1564,9 @@ SP base_params(const float* logits, const float* q, const float* u, int B, int R
   prm.R = R;
   prm.V = V;
   prm.T = cfg->temperature > 0.f ? cfg->temperature : 1.f;
-  prm.invT = 1.0f / prm.T;
+  const double c = 1.0 / ((double)prm.T * 0.6931471805599453);
+  prm.c_hi = (float)c;
+  prm.c_lo = (float)(c - (double)prm.c_hi);
   prm.top_k = cfg->top_k;
   prm.top_p = cfg->top_p;
   prm.greedy = cfg->greedy ? 1 : 0;
@@ -1221,6 +1581,8 @@ SP base_params(const float* logits, const float* q, const float* u, int B, int R
   prm.qbulk = (q && V % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0) ? 1 : 0;
   return prm;
 }
+
+bool slice_fits(int V) { return (size_t)slice_of(V, cluster_size(V)) * 4 <= kMaxSliceBytes; }
 
 }  // namespace
 
@@ -1244,8 +1606,8 @@ extern "C" spec_status spec_accept_sample(const float* target_logits, const floa
   if (!target_logits || !accepted_len || !emitted || !workspace) return SPEC_EINVAL;
   if (R > 1 && !draft_tokens) return SPEC_EINVAL;
   if (!cfg->greedy && (!uniforms || (R > 1 && !draft_probs))) return SPEC_EINVAL;
-  if (R > kMaxN || B * R > 65535) return SPEC_EUNSUPPORTED;
-  if (plan_sampler(V).smem > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
+  if (R > kMaxN || (long long)B * R * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
+  if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
   size_t a, c;
   if (workspace_bytes < samp_ws(B, R, &a, &c)) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;
@@ -1275,8 +1637,8 @@ extern "C" spec_status spec_accept_sample_tree(const float* target_logits,
       !workspace)
     return SPEC_EINVAL;
   if (!cfg->greedy && (!uniforms || !draft_probs)) return SPEC_EINVAL;
-  if (N > kMaxN || B * N > 65535) return SPEC_EUNSUPPORTED;
-  if (plan_sampler(V).smem > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
+  if (N > kMaxN || (long long)B * N * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
+  if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
   size_t a, c;
   if (workspace_bytes < samp_ws(B, N, &a, &c)) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;
