@@ -29,7 +29,6 @@
 namespace {
 
 constexpr int kStageTokens = 64;       // granularity of chunks (and the fp32 path)
-constexpr int kMaxStages = 6;
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps;
@@ -125,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
     // through 16-byte cp.async (L2 -> shared, L1 bypassed) into the swizzled
     // stage layout; each thread's copies complete on the stage's mbarrier.
     const int pt = threadIdx.x - 32 * kConsumerWarps;   // 0 .. 127
-    static_assert(kProducerThreads == 128, "16 columns x 8 token lanes");
+    static_assert(kProducerThreads == 128, "4 column groups x 32 token lanes");
     const int P = p.page_size;
     const int pg0 = c0 / P;
     const int npg = (c1 - 1) / P - pg0 + 1;
@@ -134,24 +133,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
     for (int i = pt; i < npg; i += kProducerThreads)
       bt_s[i] = (pg0 + i < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + pg0 + i] : -1;
     asm volatile("bar.sync 2, %0;" ::"n"(kProducerThreads) : "memory");
-    // Thread pt owns 16-byte column ch of token lanes tl, tl + 8, ..., tl + 56
-    // of every stage (K and V): its swizzled column offset is fixed, a page
-    // lookup is needed once per token, and each copy is two adds.
-    const int ch = pt & 15, tl = pt >> 4;
-    const uint32_t col = (uint32_t)((ch >> 3) * H + (((ch & 7) ^ tl) << 4));
+    // Thread pt copies 64 contiguous bytes (16-byte columns 4 c4 .. 4 c4 + 3)
+    // of token lanes tl, tl + 32, ... of every stage, K and V: one page lookup
+    // per token, and the four swizzled column offsets are fixed per thread (a
+    // token's swizzle depends only on tl & 7).  A warp covers 8 whole 256-byte
+    // rows per instruction.
+    const int c4 = pt & 3, tl = pt >> 2;
+    uint32_t col[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int ch = 4 * c4 + u;
+      col[u] = (uint32_t)((ch >> 3) * H + (((ch & 7) ^ (tl & 7)) << 4));
+    }
     const size_t tok_stride = (size_t)p.Hkv * 256;   // bytes between consecutive cache rows
-    const uint8_t* kcol = reinterpret_cast<const uint8_t*>(p.k) + (size_t)kvh * 256 + ch * 16;
-    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(p.v) + (size_t)kvh * 256 + ch * 16;
+    const uint8_t* kcol = reinterpret_cast<const uint8_t*>(p.k) + (size_t)kvh * 256 + c4 * 64;
+    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(p.v) + (size_t)kvh * 256 + c4 * 64;
     const bool pow2 = (P & (P - 1)) == 0;
     const int pshift = __ffs(P) - 1;
     for (int k = 0; k < nst; ++k) {
       const int slot = k % kNumStages;
       if (k >= kNumStages && !mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err)) break;
-      const uint32_t dst0 = smem_u32(stages + slot * kStageBytes) + col + tl * 128;
-      const int t0 = c0 + k * ST + tl;
+      const uint32_t sbase = smem_u32(stages + slot * kStageBytes);
 #pragma unroll
-      for (int j = 0; j < ST / 8; ++j) {
-        const int t = t0 + 8 * j;
+      for (int j = 0; j < ST / 32; ++j) {
+        const int tok = tl + 32 * j;   // token within the stage
+        const int t = c0 + k * ST + tok;
         int pg = -1, slotp = 0;
         if (t < kv_len) {
           const int pi = pow2 ? (t >> pshift) : (t / P);
@@ -161,13 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
         const bool ok = pg >= 0 && pg < p.num_pages;
         const size_t row = ok ? ((size_t)pg * P + slotp) * tok_stride : 0;
         const uint32_t n = ok ? 16u : 0u;   // positions past the sequence / bad pages: zeros
-        const uint32_t dst = dst0 + j * 1024;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(kcol + row),
-                     "r"(n)
-                     : "memory");
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 2 * H),
-                     "l"(vcol + row), "r"(n)
-                     : "memory");
+        const uint32_t drow = sbase + tok * 128;
+        const uint8_t* ks = kcol + row;
+        const uint8_t* vs = vcol + row;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(drow + col[u]),
+                       "l"(ks + 16 * u), "r"(n)
+                       : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(drow + col[u] + 2 * H),
+                       "l"(vs + 16 * u), "r"(n)
+                       : "memory");
+        }
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
                        smem_u32(&full[slot]))

@@ -68,16 +68,33 @@ SPEC_DEV uint64_t global_ns() {
   return t;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (returns as soon as it completes).
+SPEC_DEV bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false (and records an error) if the phase does not
-// complete within SPEC_WAIT_NS.
+// complete within SPEC_WAIT_NS.  The fast path touches no global memory: it
+// polls with suspended waits; only a wait that has already lasted long checks
+// the clock and whether another wait of this launch has given up.
 SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  // once any wait of this launch has given up, later waits give up at once
-  if (err && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
+  for (int it = 0; it < 64; ++it)
+    if (mbar_try_wait_ns(bar, parity, 1000)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
+    // once any wait of this launch has given up, later waits give up at once
+    if (err && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
     for (int it = 0; it < 256; ++it)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_ns(bar, parity, 1000)) return true;
     if (global_ns() - t0 > SPEC_WAIT_NS) break;
   }
   set_error(err, SPEC_ERR_MBAR_TIMEOUT);
