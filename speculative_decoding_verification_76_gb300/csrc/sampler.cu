@@ -126,6 +126,8 @@ struct Sh {
   int tok[kMaxN];
   float invw_used[kMaxN];
   Outcome outs[kMaxN];
+  int cpos[kMaxN];  // list position of each child's token (-1: not kept)
+  float eprobe;
   int token_in;
   uint64_t bar;
 };
@@ -666,8 +668,8 @@ SPEC_DEV int nth_in_cluster(int n, int lo, int nth, Pred pred, int rank, int CS,
 }
 
 // tau / tie of the top-k then top-p cut by exact radix selection; E in buf.
-template <int NT>
-SPEC_DEV Cut cut_radix(const SP& p, const float* lrow, const float* buf, int n, int lo,
+template <int NT, class EK>
+SPEC_DEV Cut cut_radix(const SP& p, const float* lrow, EK ek, int n, int lo,
                        const RadixScratch& rs, int rank, int CS, int& ph, Sh<NT / 32>& sh) {
   Cut c{2, 0.f, 0u, INT_MAX};
   if (p.top_k > 0 && p.top_k < p.V) {
@@ -689,7 +691,7 @@ SPEC_DEV Cut cut_radix(const SP& p, const float* lrow, const float* buf, int n, 
     const int tc = c.tie;
     auto keep_k = [&](int k, uint32_t key) { return is_kept(key, lo + k, tk, tc); };
     auto mass = [&](int k) {
-      return (unsigned long long)__float2ull_rn(buf[k] * 1099511627776.0f);  // 2^40
+      return (unsigned long long)__float2ull_rn(ek(k) * 1099511627776.0f);  // 2^40
     };
     const Sel s = radix_select<NT>(lrow, n, true, (double)p.top_p, 0ull, keep_k, mass, rs, CS);
     const unsigned long long e_tau = s.at_count ? s.at_weight / s.at_count : 0ull;
@@ -721,6 +723,273 @@ SPEC_DEV int next_child(const int* par, int v, int c, int R) {
   for (int c2 = c + 1; c2 < R; ++c2)
     if (par[c2] == v) return c2;
   return -1;
+}
+
+// ---------------------------------------------------------------- the bin range of the cut
+// Warp 0: the bin range [b_lo, b_hi] the top-k / top-p cut can fall in, from
+// the octave totals (octf(o, count, m16 sum); lane = octave) and the bins of
+// the octaves the crossings fall in (binf(b, count, m16 sum); lane = bin
+// within the octave).  mode 1: found; 2: use the exact radix selection.
+// kidx: the top-k cut's index among the members (-1: no top-k); members: the
+// count in the range (-1: not known from the histogram).
+template <int NT, class OctF, class BinF>
+SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, double zall, OctF octf,
+                         BinF binf, int* mode_o, int* b_lo_o, int* b_hi_o, int* kidx_o) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long oc_c = 0, oc_m = 0;
+  octf(lane, oc_c, oc_m);
+  oc_m = bin_fx(oc_m, 32 * lane);  // all bins of an octave share one exponent
+  unsigned long long xc = oc_c, xm = oc_m;  // inclusive scans over octaves
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long tc = __shfl_up_sync(kFull, xc, o);
+    const unsigned long long tmv = __shfl_up_sync(kFull, xm, o);
+    if (lane >= o) { xc += tc; xm += tmv; }
+  }
+  const unsigned long long pc = xc - oc_c, pm = xm - oc_m;  // before each octave
+  // cluster totals of the bins of octave o (lane j: bin 32 o + j)
+  auto load_oct = [&](int o, unsigned long long& bc, unsigned long long& bmass) {
+    unsigned long long mm = 0;
+    bc = 0;
+    binf(32 * o + lane, bc, mm);
+    bmass = bin_fx(mm, 32 * o);
+  };
+  // inclusive scan over the lanes
+  auto scan = [&](unsigned long long v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += t;
+    }
+    return v;
+  };
+  // first lane where po + running value reaches thr (31 if none)
+  auto first_at = [&](unsigned long long po, unsigned long long incl,
+                      unsigned long long thr) -> int {
+    const unsigned h = __ballot_sync(kFull, po + incl >= thr);
+    return h ? __ffs(h) - 1 : 31;
+  };
+  int mode = 1, b_lo = 0, b_hi = 0, kidx = -1, members = -1;
+  if (topk) {
+    const unsigned h = __ballot_sync(kFull, xc >= (unsigned long long)top_k);
+    if (!h) {
+      mode = 2;  // the k-th largest lies below 2^-32 of the maximum
+    } else {
+      const int ok = __ffs(h) - 1;
+      unsigned long long bc, bmass;
+      load_oct(ok, bc, bmass);
+      const unsigned long long ic = scan(bc);
+      const unsigned long long pck = __shfl_sync(kFull, pc, ok);
+      const int jk = first_at(pck, ic, (unsigned long long)top_k);
+      const int bk = 32 * ok + jk;
+      b_lo = b_hi = bk;
+      const int cnt_before_bk = (int)(pck + __shfl_sync(kFull, ic - bc, jk));
+      kidx = top_k - cnt_before_bk - 1;
+      members = (int)__shfl_sync(kFull, bc, jk);
+      if (topp) {
+        // the mass above bk, then the bin where top_p times it is reached
+        const unsigned long long im = scan(bmass);
+        const unsigned long long abk =
+            __shfl_sync(kFull, pm, ok) + __shfl_sync(kFull, im - bmass, jk);
+        const unsigned long long thr = (unsigned long long)((double)top_p * (double)abk);
+        const unsigned h2 = __ballot_sync(kFull, xm >= thr);
+        int ol = h2 ? __ffs(h2) - 1 : ok;
+        if (ol > ok) ol = ok;
+        unsigned long long lc = bc, lm = bmass, ilc = ic, ilm = im;
+        if (ol != ok) {
+          load_oct(ol, lc, lm);
+          ilc = scan(lc);
+          ilm = scan(lm);
+        }
+        int bl = 32 * ol + first_at(__shfl_sync(kFull, pm, ol), ilm, thr);
+        if (bl > bk) bl = bk;
+        b_lo = bl;
+        // members in [b_lo, bk], and the count above b_lo
+        const int jl = bl - 32 * ol;
+        unsigned long long inrange;
+        if (ol == ok) {
+          inrange = (lane >= jl && lane <= jk) ? bc : 0;
+        } else {
+          inrange = (lane >= jl ? lc : 0) + (lane <= jk ? bc : 0) +
+                    ((lane > ol && lane < ok) ? oc_c : 0);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) inrange += __shfl_xor_sync(kFull, inrange, o);
+        members = (int)inrange;
+        const int cnt_before_bl =
+            (int)(__shfl_sync(kFull, pc, ol) + __shfl_sync(kFull, ilc - lc, jl));
+        kidx = top_k - cnt_before_bl - 1;
+      }
+    }
+  } else {
+    const double zd = zall;
+    const unsigned long long thr = (unsigned long long)((double)top_p * zd * kFx);
+    const unsigned h = __ballot_sync(kFull, xm >= thr);
+    if (!h) {
+      mode = 2;
+    } else {
+      const int ol = __ffs(h) - 1;
+      unsigned long long bc, bmass;
+      load_oct(ol, bc, bmass);
+      const int jl = first_at(__shfl_sync(kFull, pm, ol), scan(bmass), thr);
+      b_lo = b_hi = 32 * ol + jl;
+    }
+  }
+  if (mode == 1 && members > NT) mode = 2;  // the selection sorts at most NT members
+  *mode_o = mode;
+  *b_lo_o = b_lo;
+  *b_hi_o = b_hi;
+  *kidx_o = kidx;
+}
+
+// ---------------------------------------------------------------- the cut among the members
+// Threads t < total hold member t (logit key, E bits), unsorted.  Sorts the
+// members by key, descending (= logit desc, id asc), with shuffles inside a
+// warp and shared memory (xkey / xbits, >= NT entries) across warps, then
+// finds the cut on exact masses (units of 2^-44) running from a_lo, the mass
+// above the members: the top-k member kidx (-1: no top-k), then (top-p) the
+// first running mass >= top_p * Z_k.  Returns false if the cut does not lie
+// among the members.
+template <int NT>
+SPEC_DEV bool select_cut(unsigned long long key, uint32_t eb, int total, unsigned long long a_lo,
+                         int kidx, bool topp, float top_p, unsigned long long zall_fx,
+                         unsigned long long* xkey, uint32_t* xbits, Cut* cut, float* zkept,
+                         Sh<NT / 32>& sh) {
+  const int t = threadIdx.x;
+  int P = 1;
+  while (P < total) P <<= 1;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      unsigned long long ok2;
+      uint32_t ob;
+      if (stride >= 32) {
+        if (t < P) {
+          xkey[t] = key;
+          xbits[t] = eb;
+        }
+        __syncthreads();
+        ok2 = (t < P) ? xkey[t ^ stride] : 0ull;
+        ob = (t < P) ? xbits[t ^ stride] : 0u;
+        __syncthreads();
+      } else {
+        ok2 = __shfl_xor_sync(kFull, key, stride);
+        ob = __shfl_xor_sync(kFull, eb, stride);
+      }
+      const bool desc = (t & size) == 0;
+      const bool lower = (t & stride) == 0;
+      const bool take = lower ? (desc ? ok2 > key : ok2 < key) : (desc ? ok2 < key : ok2 > key);
+      if (take) {
+        key = ok2;
+        eb = ob;
+      }
+    }
+  }
+  // thread t now holds the t-th largest member
+  const bool live = t < total;
+  const unsigned long long mt = live ? fx44(eb) : 0ull;
+  const unsigned long long incl = a_lo + block_incl_scan_u64<NT>(mt, sh);  // mass through t
+  const int last = (kidx >= 0) ? min(kidx, total - 1) : total - 1;
+  if (t == 0) {
+    sh.bi[5] = 0;
+    if (kidx < 0) sh.zk = zall_fx;
+  }
+  __syncthreads();
+  if (kidx >= 0 && t == last) sh.zk = incl;  // Z after top-k
+  __syncthreads();
+  const unsigned long long zk = sh.zk;
+  int pick = -1;
+  if (!topp) {
+    if (t == last) pick = t;
+  } else {
+    const unsigned long long thr = (unsigned long long)((double)top_p * (double)zk);
+    if (live && t <= last && incl - mt < thr && incl >= thr) pick = t;
+  }
+  if (pick >= 0) {  // unique: masses are positive
+    sh.cut = Cut{1, __uint_as_float(eb), (uint32_t)(key >> 32), (int)(0xFFFFFFFFu - (uint32_t)key)};
+    sh.zcut = incl;
+    sh.bi[5] = 1;
+  }
+  __syncthreads();
+  const bool ok = sh.bi[5] != 0;
+  if (ok) {
+    *cut = sh.cut;
+    *zkept = (float)sh.zcut * (1.0f / 17592186044416.0f);  // 2^-44
+  }
+  __syncthreads();
+  return ok;
+}
+
+// ---------------------------------------------------------------- row outcome
+// Warp 0 of the row's (rank-0) CTA publishes the row's outcome; the warp that
+// brings the sequence's counter to R assembles accepted_len, emitted, path
+// and status from the R outcomes and resets the counter.
+template <int NW>
+SPEC_DEV void finish_row(const SP& p, int row, const Outcome& oc, Sh<NW>& sh) {
+  const int lane = threadIdx.x & 31;
+  const int R = p.R;
+  const int b = row / R;
+  int last = 0;
+  if (lane == 0) {
+    p.outcomes[row] = oc;
+    __threadfence();
+    last = atomicAdd(&p.seq_count[b], 1) == R - 1;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence();
+  // warp 0 loads the sequence's outcomes (and its draft tokens) in parallel
+  for (int r = lane; r < R; r += 32) {
+    const int4 v = __ldcg(reinterpret_cast<const int4*>(&p.outcomes[(size_t)b * R + r]));
+    sh.outs[r] = Outcome{v.x, v.y, v.z, v.w};
+    sh.tok[r] = p.tree ? __ldg(&p.tokens[(size_t)b * R + r])
+                       : (r < R - 1 ? __ldg(&p.tokens[(size_t)b * (R - 1) + r]) : -1);
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  int32_t* emitted = p.emitted + (size_t)b * R;
+  int nonfin = 0, status = 0, acc = 0, k = 0;
+  for (int r = 0; r < R; ++r) nonfin |= sh.outs[r].flags;
+  if (nonfin) {
+    acc = -1;
+    status = SPEC_SEQ_NONFINITE;
+  } else if (!p.tree) {
+    for (int r = 0; r < R; ++r) {
+      const Outcome& o = sh.outs[r];
+      status |= o.status;
+      if (r < R - 1 && o.accept) {
+        const int x = sh.tok[r];
+        emitted[k++] = x;
+        ++acc;
+        if (x == p.eos) break;
+        continue;
+      }
+      emitted[k++] = o.token;
+      break;
+    }
+  } else {
+    int32_t* path = p.path + (size_t)b * R;
+    int v = 0;
+    while (true) {
+      const Outcome& o = sh.outs[v];
+      status |= o.status;
+      if (o.accept > v) {
+        const int t = sh.tok[o.accept];
+        emitted[k++] = t;
+        path[acc++] = o.accept;
+        v = o.accept;
+        if (t == p.eos) break;
+        continue;
+      }
+      emitted[k++] = o.token;
+      break;
+    }
+  }
+  for (int c = (nonfin ? 0 : k); c < R; ++c) emitted[c] = -1;
+  if (p.tree)
+    for (int c = (nonfin ? 0 : acc); c < R; ++c) p.path[(size_t)b * R + c] = -1;
+  p.acc_len[b] = acc;
+  if (p.status) p.status[b] = status;
+  p.seq_count[b] = 0;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -954,117 +1223,27 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       // the cluster (lane = octave), then the bins of the octaves the
       // crossings fall in (lane = bin within the octave)
       if (warp == 0) {
-        unsigned long long oc_c = 0, oc_m = 0;
-        for (int r = 0; r < CS; ++r) {
-          if (topk) oc_c += dsmem_ld_u32(&sh.oct[lane], r);
-          if (topp) oc_m += dsmem_ld_u32(&sh.oct[32 + lane], r);
-        }
-        oc_m = bin_fx(oc_m, 32 * lane);  // all bins of an octave share one exponent
-        unsigned long long xc = oc_c, xm = oc_m;  // inclusive scans over octaves
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long tc = __shfl_up_sync(kFull, xc, o);
-          const unsigned long long tmv = __shfl_up_sync(kFull, xm, o);
-          if (lane >= o) { xc += tc; xm += tmv; }
-        }
-        const unsigned long long pc = xc - oc_c, pm = xm - oc_m;  // before each octave
-        // cluster totals of the bins of octave o (lane j: bin 32 o + j)
-        auto load_oct = [&](int o, unsigned long long& bc, unsigned long long& bmass) {
-          bc = 0;
-          unsigned long long mm = 0;
-          for (int r = 0; r < CS; ++r) {
-            if (topk) bc += dsmem_ld_u32(&hcnt[32 * o + lane], r);
-            if (topp) mm += dsmem_ld_u32(&hm[32 * o + lane], r);
-          }
-          bmass = bin_fx(mm, 32 * o);
-        };
-        // inclusive scan over the lanes
-        auto scan = [&](unsigned long long v) {
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long t = __shfl_up_sync(kFull, v, o);
-            if (lane >= o) v += t;
-          }
-          return v;
-        };
-        // first lane where po + running value reaches thr (31 if none)
-        auto first_at = [&](unsigned long long po, unsigned long long incl,
-                            unsigned long long thr) -> int {
-          const unsigned h = __ballot_sync(kFull, po + incl >= thr);
-          return h ? __ffs(h) - 1 : 31;
-        };
-        int mode = 1, b_lo = 0, b_hi = 0, kidx = -1, members = -1;
-        if (topk) {
-          const unsigned h = __ballot_sync(kFull, xc >= (unsigned long long)p.top_k);
-          if (!h) {
-            mode = 2;  // the k-th largest lies below 2^-32 of the maximum
-          } else {
-            const int ok = __ffs(h) - 1;
-            unsigned long long bc, bmass;
-            load_oct(ok, bc, bmass);
-            const unsigned long long ic = scan(bc);
-            const unsigned long long pck = __shfl_sync(kFull, pc, ok);
-            const int jk = first_at(pck, ic, (unsigned long long)p.top_k);
-            const int bk = 32 * ok + jk;
-            b_lo = b_hi = bk;
-            const int cnt_before_bk = (int)(pck + __shfl_sync(kFull, ic - bc, jk));
-            kidx = p.top_k - cnt_before_bk - 1;
-            members = (int)__shfl_sync(kFull, bc, jk);
-            if (topp) {
-              // the mass above bk, then the bin where top_p times it is reached
-              const unsigned long long im = scan(bmass);
-              const unsigned long long abk =
-                  __shfl_sync(kFull, pm, ok) + __shfl_sync(kFull, im - bmass, jk);
-              const unsigned long long thr = (unsigned long long)((double)p.top_p * (double)abk);
-              const unsigned h2 = __ballot_sync(kFull, xm >= thr);
-              int ol = h2 ? __ffs(h2) - 1 : ok;
-              if (ol > ok) ol = ok;
-              unsigned long long lc = bc, lm = bmass, ilc = ic, ilm = im;
-              if (ol != ok) {
-                load_oct(ol, lc, lm);
-                ilc = scan(lc);
-                ilm = scan(lm);
+        int mode, bl, bh, kx;
+        find_range<NT>(
+            topk, topp, p.top_k, p.top_p, (double)zah + (double)zal,
+            [&](int o, unsigned long long& c, unsigned long long& mm) {
+              for (int r = 0; r < CS; ++r) {
+                if (topk) c += dsmem_ld_u32(&sh.oct[o], r);
+                if (topp) mm += dsmem_ld_u32(&sh.oct[32 + o], r);
               }
-              int bl = 32 * ol + first_at(__shfl_sync(kFull, pm, ol), ilm, thr);
-              if (bl > bk) bl = bk;
-              b_lo = bl;
-              // members in [b_lo, bk], and the count above b_lo
-              const int jl = bl - 32 * ol;
-              unsigned long long inrange;
-              if (ol == ok) {
-                inrange = (lane >= jl && lane <= jk) ? bc : 0;
-              } else {
-                inrange = (lane >= jl ? lc : 0) + (lane <= jk ? bc : 0) +
-                          ((lane > ol && lane < ok) ? oc_c : 0);
+            },
+            [&](int bb, unsigned long long& c, unsigned long long& mm) {
+              for (int r = 0; r < CS; ++r) {
+                if (topk) c += dsmem_ld_u32(&hcnt[bb], r);
+                if (topp) mm += dsmem_ld_u32(&hm[bb], r);
               }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) inrange += __shfl_xor_sync(kFull, inrange, o);
-              members = (int)inrange;
-              const int cnt_before_bl =
-                  (int)(__shfl_sync(kFull, pc, ol) + __shfl_sync(kFull, ilc - lc, jl));
-              kidx = p.top_k - cnt_before_bl - 1;
-            }
-          }
-        } else {
-          const double zd = (double)zah + (double)zal;
-          const unsigned long long thr = (unsigned long long)((double)p.top_p * zd * kFx);
-          const unsigned h = __ballot_sync(kFull, xm >= thr);
-          if (!h) {
-            mode = 2;
-          } else {
-            const int ol = __ffs(h) - 1;
-            unsigned long long bc, bmass;
-            load_oct(ol, bc, bmass);
-            const int jl = first_at(__shfl_sync(kFull, pm, ol), scan(bmass), thr);
-            b_lo = b_hi = 32 * ol + jl;
-          }
-        }
-        if (mode == 1 && members > NT) mode = 2;  // the selection sorts at most NT members
+            },
+            &mode, &bl, &bh, &kx);
         if (lane == 0) {
           sh.bi[0] = mode;
-          sh.bi[1] = b_lo;
-          sh.bi[2] = b_hi;
-          sh.bi[3] = kidx;
+          sh.bi[1] = bl;
+          sh.bi[2] = bh;
+          sh.bi[3] = kx;
         }
       }
       __syncthreads();
@@ -1132,76 +1311,16 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
               off += cr;
             }
           }
-          int P = 1;
-          while (P < total) P <<= 1;
-          // bitonic sort, descending key (= logit desc, id asc): shuffles within
-          // a warp, shared memory across warps
-          for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-              unsigned long long ok2;
-              uint32_t ob;
-              if (stride >= 32) {
-                if (t < P) {
-                  gkey[t] = key;
-                  gbits[t] = eb;
-                }
-                __syncthreads();
-                ok2 = (t < P) ? gkey[t ^ stride] : 0ull;
-                ob = (t < P) ? gbits[t ^ stride] : 0u;
-                __syncthreads();
-              } else {
-                ok2 = __shfl_xor_sync(kFull, key, stride);
-                ob = __shfl_xor_sync(kFull, eb, stride);
-              }
-              const bool desc = (t & size) == 0;
-              const bool lower = (t & stride) == 0;
-              const bool take = lower ? (desc ? ok2 > key : ok2 < key) : (desc ? ok2 < key : ok2 > key);
-              if (take) {
-                key = ok2;
-                eb = ob;
-              }
-            }
-          }
-          // ---- 5b. the cut on exact masses: thread t holds the t-th largest member
-          const bool live = t < total;
-          const unsigned long long mt = live ? fx44(eb) : 0ull;
-          const unsigned long long incl = a_lo + block_incl_scan_u64<NT>(mt, sh);  // mass through t
-          const int last = (kidx >= 0) ? min(kidx, total - 1) : total - 1;
-          if (threadIdx.x == 0) {
-            sh.bi[5] = 0;
-            if (kidx < 0) sh.zk = (unsigned long long)(((double)zah + (double)zal) * kFx);
-          }
-          __syncthreads();
-          if (kidx >= 0 && t == last) sh.zk = incl;  // Z after top-k
-          __syncthreads();
-          const unsigned long long zk = sh.zk;
-          int pick = -1;
-          if (!topp) {
-            if (t == last) pick = t;
-          } else {
-            const unsigned long long thr = (unsigned long long)((double)p.top_p * (double)zk);
-            if (live && t <= last && incl - mt < thr && incl >= thr) pick = t;
-          }
-          if (pick >= 0) {  // unique: masses are positive
-            sh.cut = Cut{1, __uint_as_float(eb), (uint32_t)(key >> 32),
-                         (int)(0xFFFFFFFFu - (uint32_t)key)};
-            sh.zcut = incl;
-            sh.bi[5] = 1;
-          }
-          __syncthreads();
-          if (sh.bi[5]) {
-            cut = sh.cut;
-            zkept = (float)sh.zcut * (1.0f / 17592186044416.0f);  // 2^-44
-          } else {
+          if (!select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
+                              (unsigned long long)(((double)zah + (double)zal) * kFx), gkey, gbits,
+                              &cut, &zkept, sh))
             tmode = 2;  // the rounded bin masses placed the cut one bin off
-          }
-          __syncthreads();
         }
       }
       if (tmode == 2) {
         // ---- 5'. exact radix selection over the logit keys
         cluster_sync();  // every CTA is done reading the others' member lists
-        cut = cut_radix<NT>(p, lrow, buf, n, lo, rs, rank, CS, ph, sh);
+        cut = cut_radix<NT>(p, lrow, [&](int k) { return buf[k]; }, n, lo, rs, rank, CS, ph, sh);
         // Z over the kept set (compensated per thread, fixed order)
         float s = 0.f, cmp = 0.f;
         for (int k = threadIdx.x; k < n; k += NT) {
@@ -1399,68 +1518,497 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   cluster_sync();  // also: no CTA leaves while another may read its shared memory
   if (rank != 0 || threadIdx.x >= 32) return;
   if (drew) oc.token = sh.token_in;
-  int last = 0;
-  if (lane == 0) {
-    p.outcomes[row] = oc;
-    __threadfence();
-    last = atomicAdd(&p.seq_count[b], 1) == R - 1;
-  }
-  last = __shfl_sync(kFull, last, 0);
-  if (!last) return;
-  __threadfence();
-  // warp 0 loads the sequence's outcomes (and its draft tokens) in parallel
-  for (int r = lane; r < R; r += 32) {
-    const int4 v = __ldcg(reinterpret_cast<const int4*>(&p.outcomes[(size_t)b * R + r]));
-    sh.outs[r] = Outcome{v.x, v.y, v.z, v.w};
-    sh.tok[r] = p.tree ? __ldg(&p.tokens[(size_t)b * R + r])
-                       : (r < R - 1 ? __ldg(&p.tokens[(size_t)b * (R - 1) + r]) : -1);
-  }
-  __syncwarp();
-  if (lane != 0) return;
-  int32_t* emitted = p.emitted + (size_t)b * R;
-  int nonfin = 0, status = 0, acc = 0, k = 0;
-  for (int r = 0; r < R; ++r) nonfin |= sh.outs[r].flags;
-  if (nonfin) {
-    acc = -1;
-    status = SPEC_SEQ_NONFINITE;
-  } else if (!p.tree) {
-    for (int r = 0; r < R; ++r) {
-      const Outcome& o = sh.outs[r];
-      status |= o.status;
-      if (r < R - 1 && o.accept) {
-        const int x = sh.tok[r];
-        emitted[k++] = x;
-        ++acc;
-        if (x == p.eos) break;
-        continue;
+  finish_row(p, row, oc, sh);
+}
+
+// ---------------------------------------------------------------- streaming kernel (many rows)
+// One 1024-thread CTA per target row, used for truncated sampling when many
+// rows run at once.  The row is read from global memory: once from HBM for
+// the maximum, then (E recomputed, the row now in L2) for Z and the
+// histogram, and for the members of the crossing bins.  The kept set (ids and
+// E) is then listed per warp in shared memory for the draws and the tree's
+// residuals.  No cluster exchanges: every SM works on its own rows.
+constexpr int kSNT = 1024;
+constexpr int kSCap = 16384;  // kept positions listed per row (kSCap / 32 per warp)
+
+__global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
+  constexpr int NT = kSNT, NW = NT / 32, WCAP = kSCap / NW;
+  extern __shared__ __align__(16) uint8_t dyn[];
+  uint32_t* hcnt = reinterpret_cast<uint32_t*>(dyn);
+  uint32_t* hm = hcnt + kHistPad;
+  unsigned long long* xkey = reinterpret_cast<unsigned long long*>(hm + kHistPad);  // NT
+  uint32_t* xbits = reinterpret_cast<uint32_t*>(xkey + NT);                          // NT
+  int* lid = reinterpret_cast<int*>(xbits + NT);                                      // kSCap
+  float* lval = reinterpret_cast<float*>(lid + kSCap);                                // kSCap
+  const RadixScratch rs{reinterpret_cast<uint32_t*>(xkey), xkey + 256, xkey + 768,
+                        reinterpret_cast<uint32_t*>(xkey) + 2048};
+  __shared__ Sh<NW> sh;
+
+  const int row = blockIdx.x;
+  const int R = p.R, V = p.V;
+  const int b = row / R;
+  const int i = row % R;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* lrow = p.logits + (size_t)row * V;
+  const bool topk = p.top_k > 0 && p.top_k < V;
+  const bool topp = p.top_p > 0.f && p.top_p < 1.f;
+  const bool trunc = topk || topp;
+  const bool vec = p.bulk != 0;  // V % 4 == 0 and 16-byte aligned rows
+  const int n4 = vec ? V / 4 : 0;
+  const float4* l4 = reinterpret_cast<const float4*>(lrow);
+  // every element of the row once: visit(k, l), four 16-byte loads in flight per thread
+  auto sweep = [&](auto&& visit) {
+    for (int base = threadIdx.x; base < n4; base += 4 * NT) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k4 = base + u * NT;
+        v[u] = k4 < n4 ? __ldg(l4 + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      emitted[k++] = o.token;
-      break;
-    }
-  } else {
-    int32_t* path = p.path + (size_t)b * R;
-    int v = 0;
-    while (true) {
-      const Outcome& o = sh.outs[v];
-      status |= o.status;
-      if (o.accept > v) {
-        const int t = sh.tok[o.accept];
-        emitted[k++] = t;
-        path[acc++] = o.accept;
-        v = o.accept;
-        if (t == p.eos) break;
-        continue;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k4 = base + u * NT;
+        if (k4 < n4) {
+          visit(4 * k4, v[u].x);
+          visit(4 * k4 + 1, v[u].y);
+          visit(4 * k4 + 2, v[u].z);
+          visit(4 * k4 + 3, v[u].w);
+        }
       }
-      emitted[k++] = o.token;
-      break;
     }
+    for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) visit(k, __ldg(lrow + k));
+  };
+  int ph = 0;
+
+  // ---- 0. setup
+  if (threadIdx.x == 0) {
+    sh.token_in = -1;
+    sh.eprobe = 0.f;
   }
-  for (int c = (nonfin ? 0 : k); c < R; ++c) emitted[c] = -1;
+  if (trunc)
+    for (int k = threadIdx.x; k < kHist; k += NT) {
+      hcnt[k] = 0u;
+      hm[k] = 0u;
+    }
   if (p.tree)
-    for (int c = (nonfin ? 0 : acc); c < R; ++c) p.path[(size_t)b * R + c] = -1;
-  p.acc_len[b] = acc;
-  if (p.status) p.status[b] = status;
-  p.seq_count[b] = 0;
+    for (int c = threadIdx.x; c < R; c += NT) {
+      sh.par[c] = p.parent[(size_t)b * R + c];
+      sh.tok[c] = p.tokens[(size_t)b * R + c];
+      sh.cpos[c] = -1;
+    }
+  __syncthreads();
+  int probe = -1;
+  if (!p.tree) {
+    if (i < R - 1) probe = __ldg(&p.tokens[(size_t)b * (R - 1) + i]);
+  } else {
+    const int fc = next_child(sh.par, i, i, R);
+    if (fc >= 0) probe = sh.tok[fc];
+  }
+  const float* qrow = nullptr;
+  if (p.q) {
+    if (p.tree)
+      qrow = p.q + ((size_t)b * R + i) * V;
+    else if (i < R - 1)
+      qrow = p.q + ((size_t)b * (R - 1) + i) * V;
+  }
+
+  // ---- 1. maximum (NaN-propagating)
+  float mx = -INFINITY;
+  sweep([&](int, float l) { mx = fmax_nan(mx, l); });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
+  if (lane == 0) sh.red_f[warp] = mx;
+  __syncthreads();
+  float m = sh.red_f[0];
+  for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.red_f[w]);
+  __syncthreads();
+  const bool bad = isnan(m) || m == INFINITY || m == -INFINITY;
+  Outcome oc{0, -1, 0, bad ? 1 : 0};
+
+  if (!bad) {
+    // ---- 2. Z (E recomputed, compensated per thread), histogram, probe value
+    const float nm = -m, lfloor = m - 150.f * p.T;
+    const float c_hi = p.c_hi, c_lo = p.c_lo;
+    auto Eof = [&](float l) { return texp(l, nm, lfloor, c_hi, c_lo); };
+    float zs = 0.f, zc = 0.f;
+    auto visit2 = [&](int k, float l) {
+      const float e = Eof(l);
+      const float y = e - zc;
+      const float t = zs + y;
+      zc = (t - zs) - y;
+      zs = t;
+      if (k == probe) sh.eprobe = e;
+      if (trunc) {
+        const uint32_t bits = __float_as_uint(e);
+        const int bn = ebin(bits);
+        if (topk) atomicAdd(&hcnt[bn], 1u);
+        if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+      }
+    };
+    sweep(visit2);
+    const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
+    const float zl = block_sum_f<NT>(-zc, sh);
+    const float e_probe = sh.eprobe;
+    const double zall = (double)zh + (double)zl;
+
+    Cut cut{0, 0.f, 0u, INT_MAX};
+    float zkept = zh + zl;
+    if (trunc) {
+      // ---- 3. the cut: bin range, members, selection (or the radix fallback)
+      if (warp == 0) {
+        int mode, bl, bh, kx;
+        find_range<NT>(
+            topk, topp, p.top_k, p.top_p, zall,
+            [&](int o, unsigned long long& c, unsigned long long& mm) {
+              for (int j = 0; j < 32; ++j) {
+                if (topk) c += hcnt[32 * o + j];
+                if (topp) mm += hm[32 * o + j];
+              }
+            },
+            [&](int bb, unsigned long long& c, unsigned long long& mm) {
+              if (topk) c += hcnt[bb];
+              if (topp) mm += hm[bb];
+            },
+            &mode, &bl, &bh, &kx);
+        if (lane == 0) {
+          sh.bi[0] = mode;
+          sh.bi[1] = bl;
+          sh.bi[2] = bh;
+          sh.bi[3] = kx;
+          sh.bi[4] = 0;
+        }
+      }
+      __syncthreads();
+      int tmode = sh.bi[0];
+      const int b_lo = sh.bi[1], b_hi = sh.bi[2], kidx = sh.bi[3];
+      if (tmode == 1) {
+        // members of bins [b_lo, b_hi] and the exact mass above them; a logit
+        // pre-filter (with margin) skips the E of elements below the range
+        const uint32_t edge = (uint32_t)(0x3F7FFFFF - ((b_hi + 1) << 18) + 1);
+        const float lpre = m + p.T * (__logf(__uint_as_float(edge)) - 1e-3f);
+        unsigned long long above = 0;
+        auto visit3 = [&](int k, float l) {
+          if (!(l >= lpre)) return;
+          const uint32_t bits = __float_as_uint(Eof(l));
+          if (bits < edge) return;
+          const int bn = ebin(bits);
+          if (bn < b_lo) {
+            above += fx44(bits);
+          } else {
+            const int slot = atomicAdd(&sh.bi[4], 1);
+            if (slot < NT) {
+              xkey[slot] = ((unsigned long long)okey(l) << 32) | (0xFFFFFFFFu - (uint32_t)k);
+              xbits[slot] = bits;
+            }
+          }
+        };
+        sweep(visit3);
+        const unsigned long long a_lo = block_sum_u64<NT>(above, sh);  // barriers: members complete
+        const int total = sh.bi[4];
+        if (total > NT || total < 1) {
+          tmode = 2;
+        } else {
+          const int t = threadIdx.x;
+          const unsigned long long key = t < total ? xkey[t] : 0ull;
+          const uint32_t eb = t < total ? xbits[t] : 0u;
+          if (!select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
+                              (unsigned long long)(zall * kFx), xkey, xbits, &cut, &zkept, sh))
+            tmode = 2;
+        }
+      }
+      if (tmode == 2) {
+        cut = cut_radix<NT>(p, lrow, [&](int k) { return Eof(__ldg(lrow + k)); }, V, 0, rs, 0, 1,
+                            ph, sh);
+        float s = 0.f, cmp = 0.f;
+        for (int k = threadIdx.x; k < V; k += NT) {
+          const float l = __ldg(lrow + k);
+          if (is_kept(okey(l), k, cut.tau, cut.tie)) {
+            const float y = Eof(l) - cmp;
+            const float tt = s + y;
+            cmp = (tt - s) - y;
+            s = tt;
+          }
+        }
+        const float hs = block_sum_f<NT>(s, sh);
+        const float ls = block_sum_f<NT>(-cmp, sh);
+        zkept = hs + ls;
+      }
+      cut.mode = 2;  // from here on the kept test uses the logit keys
+    }
+    const float invz = 1.0f / zkept;
+    auto kept_l = [&](float l, int id) { return !trunc || is_kept(okey(l), id, cut.tau, cut.tie); };
+
+    // ---- 4. (on first use) list each warp's kept positions with their E
+    const int rw = ((V + NW - 1) / NW + 3) / 4 * 4;
+    const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
+    bool listed = false, list_ready = false;
+    auto ensure_list = [&]() {
+      if (list_ready) return;
+      list_ready = true;
+      int cntw = 0;
+      for (int s0 = r0; s0 < r1; s0 += 128) {
+        float lv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = s0 + 32 * u + lane;
+          lv[u] = k < r1 ? __ldg(lrow + k) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = s0 + 32 * u + lane;
+          const bool kp = k < r1 && kept_l(lv[u], k);
+          const unsigned bal = __ballot_sync(kFull, kp);
+          const int pos = cntw + __popc(bal & ((1u << lane) - 1));
+          if (kp && pos < WCAP) {
+            lid[warp * WCAP + pos] = k;
+            lval[warp * WCAP + pos] = Eof(lv[u]);
+          }
+          cntw += __popc(bal);
+        }
+      }
+      if (lane == 0) sh.list_n[warp] = cntw;
+      listed = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
+      // list positions of the node's children (binary search in the owning warp's list)
+      if (listed && p.tree)
+        for (int c = threadIdx.x; c < R; c += NT) {
+          const int t = sh.tok[c];
+          if (sh.par[c] != i || t < 0 || t >= V) continue;
+          const int w = min(t / rw, NW - 1);
+          int lo2 = 0, hi2 = sh.list_n[w];
+          while (lo2 < hi2) {
+            const int mid = (lo2 + hi2) >> 1;
+            if (lid[w * WCAP + mid] < t) lo2 = mid + 1; else hi2 = mid;
+          }
+          if (lo2 < sh.list_n[w] && lid[w * WCAP + lo2] == t) sh.cpos[c] = w * WCAP + lo2;
+        }
+      __syncthreads();
+    };
+    if (p.p_out) {
+      float* dst = p.p_out + (size_t)row * V;
+      for (int k = threadIdx.x; k < V; k += NT) {
+        const float l = __ldg(lrow + k);
+        dst[k] = kept_l(l, k) ? Eof(l) * invz : 0.f;
+      }
+    }
+
+    // weights of the listed items (mode 1: max(0, v * invw - q) stored back):
+    // per-warp sums in sh.wsum, the CTA total returned (fixed order)
+    auto list_weights = [&](int mode, float invw) -> float {
+      const int cnt = min(sh.list_n[warp], WCAP);
+      float acc = 0.f;
+      for (int j = lane; j < cnt; j += 32) {
+        float v = lval[warp * WCAP + j];
+        if (mode == 1) {
+          const float qv = v > 0.f ? __ldg(qrow + lid[warp * WCAP + j]) : 0.f;
+          v = residual_w(v, invw, qv);
+          lval[warp * WCAP + j] = v;
+        }
+        acc += v;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+      if (lane == 0) sh.wsum[warp] = acc;
+      __syncthreads();
+      float t = 0.f;
+      for (int w = 0; w < NW; ++w) t += sh.wsum[w];
+      return t;
+    };
+    // the first listed id whose running weight (ascending id) exceeds u * W
+    auto list_locate = [&](float u, float W) -> int {
+      const float target = u * W;
+      int ow = -1, lw = -1;
+      float wpre = 0.f, base_ow = 0.f, base_lw = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        const float t = sh.wsum[w];
+        if (t > 0.f) {
+          if (ow < 0 && wpre + t > target) { ow = w; base_ow = wpre; }
+          lw = w;
+          base_lw = wpre;
+        }
+        wpre += t;
+      }
+      if (ow < 0) { ow = lw; base_ow = base_lw; }
+      if (ow < 0) return -1;
+      if (warp == ow) {
+        const int cnt = min(sh.list_n[ow], WCAP);
+        const int c = ((cnt + 31) / 32) | 1;
+        const int j0 = min(lane * c, cnt), j1 = min(j0 + c, cnt);
+        float ls = 0.f;
+        for (int j = j0; j < j1; ++j) ls += lval[ow * WCAP + j];
+        const float tw = target - base_ow;
+        float incl = ls;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const unsigned hit = __ballot_sync(kFull, ls > 0.f && incl > tw);
+        const unsigned nz = __ballot_sync(kFull, ls > 0.f);
+        const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
+        int found = -1;
+        if (lane == L) {
+          const float tl = tw - (incl - ls);
+          float run = 0.f;
+          int lastk = -1;
+          for (int j = j0; j < j1; ++j) {
+            const float v = lval[ow * WCAP + j];
+            if (v > 0.f) {
+              lastk = lid[ow * WCAP + j];
+              run += v;
+              if (run > tl) { found = lastk; break; }
+            }
+          }
+          if (found < 0) found = lastk;
+        }
+        found = __shfl_sync(kFull, found, L < 0 ? 0 : L);
+        if (lane == 0) sh.bi[7] = found;
+      }
+      __syncthreads();
+      const int t = sh.bi[7];
+      __syncthreads();
+      return t;
+    };
+    // the same over the whole row with the weights recomputed (kept set too
+    // large to list): w = kept ? (mode 1: max(0, E * invz - q); mode 0: E) : 0
+    auto wfull = [&](int k, int mode) -> float {
+      const float l = __ldg(lrow + k);
+      if (!kept_l(l, k)) return 0.f;
+      const float e = Eof(l);
+      return mode == 1 ? residual_w(e, invz, __ldg(qrow + k)) : e;
+    };
+    auto full_draw = [&](int mode, float u) -> int {
+      float acc = 0.f;
+      for (int k = r0 + lane; k < r1; k += 32) acc += wfull(k, mode);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+      if (lane == 0) sh.wsum[warp] = acc;
+      __syncthreads();
+      float W = 0.f;
+      for (int w = 0; w < NW; ++w) W += sh.wsum[w];
+      if (!(W > 0.f)) return -2;
+      const float target = u * W;
+      int ow = -1, lw = -1;
+      float wpre = 0.f, base_ow = 0.f, base_lw = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        const float t = sh.wsum[w];
+        if (t > 0.f) {
+          if (ow < 0 && wpre + t > target) { ow = w; base_ow = wpre; }
+          lw = w;
+          base_lw = wpre;
+        }
+        wpre += t;
+      }
+      if (ow < 0) { ow = lw; base_ow = base_lw; }
+      if (warp == ow) {
+        const int wr0 = min(ow * rw, V), wr1 = min((ow + 1) * rw, V);
+        const int c = ((wr1 - wr0 + 31) / 32) | 1;
+        const int j0 = min(wr0 + lane * c, wr1), j1 = min(j0 + c, wr1);
+        float ls = 0.f;
+        for (int k = j0; k < j1; ++k) ls += wfull(k, mode);
+        const float tw = target - base_ow;
+        float incl = ls;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const unsigned hit = __ballot_sync(kFull, ls > 0.f && incl > tw);
+        const unsigned nz = __ballot_sync(kFull, ls > 0.f);
+        const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
+        int found = -1;
+        if (lane == L) {
+          const float tl = tw - (incl - ls);
+          float run = 0.f;
+          for (int k = j0; k < j1; ++k) {
+            const float v = wfull(k, mode);
+            if (v > 0.f) {
+              found = k;
+              run += v;
+              if (run > tl) break;
+            }
+          }
+        }
+        found = __shfl_sync(kFull, found, L < 0 ? 0 : L);
+        if (lane == 0) sh.bi[7] = found;
+      }
+      __syncthreads();
+      const int t = sh.bi[7];
+      __syncthreads();
+      return t;
+    };
+
+    const float u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    if (!p.tree) {
+      // ---- 5a. chain: the row's test, then its correction or bonus draw
+      bool resid = false;
+      if (i < R - 1) {
+        const int x = probe;
+        const bool xin = x >= 0 && x < V;
+        const float qx = xin ? __ldg(&qrow[x]) : 0.f;
+        const float px = (xin && e_probe > 0.f && kept_l(__ldg(lrow + x), x)) ? e_probe * invz : 0.f;
+        if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
+        oc.accept = (__ldg(&p.u[(size_t)b * R + i]) * qx < px) ? 1 : 0;
+        resid = !oc.accept;
+      }
+      if (i == R - 1 || resid) {
+        ensure_list();
+        int tokn;
+        if (listed) {
+          const float W = list_weights(resid ? 1 : 0, invz);
+          tokn = W > 0.f ? list_locate(u_final, W) : -2;
+        } else {
+          tokn = full_draw(resid ? 1 : 0, u_final);
+        }
+        if (tokn == -2) {  // residual with zero mass (rounding only): draw from p
+          oc.status |= SPEC_SEQ_RESID_ZERO;
+          tokn = full_draw(0, u_final);
+        }
+        oc.token = tokn;
+      }
+    } else {
+      // ---- 5b. tree node: children in storage order against the running p'
+      ensure_list();  // the host routes here only trees whose kept set fits the lists
+      oc.accept = -1;
+      float invw = invz;
+      int nsteps = 0;
+      for (int c = next_child(sh.par, i, i, R); c >= 0; c = next_child(sh.par, i, c, R)) {
+        const int t = sh.tok[c];
+        const bool tin = t >= 0 && t < V;
+        const float qt = tin ? __ldg(&qrow[t]) : 0.f;
+        const float pt = (tin && sh.cpos[c] >= 0) ? lval[sh.cpos[c]] * invw : 0.f;
+        if (qt == 0.f) oc.status |= SPEC_SEQ_QZERO;
+        if (__ldg(&p.u[(size_t)b * R + (c - 1)]) * qt < pt) {
+          oc.accept = c;
+          break;
+        }
+        if (threadIdx.x == 0) sh.invw_used[nsteps] = invw;
+        const float W = list_weights(1, invw);  // p' <- norm(max(0, p' - q_v))
+        if (W > 1e-37f) {
+          invw = 1.0f / W;
+          ++nsteps;
+        } else {
+          // zero mass (rounding only): keep p' -- rebuild it from the logits
+          oc.status |= SPEC_SEQ_RESID_ZERO;
+          const int cnt = min(sh.list_n[warp], WCAP);
+          for (int j = lane; j < cnt; j += 32) {
+            const int id = lid[warp * WCAP + j];
+            float e = Eof(__ldg(lrow + id));
+            for (int s2 = 0; s2 < nsteps; ++s2)
+              e = residual_w(e, sh.invw_used[s2], e > 0.f ? __ldg(qrow + id) : 0.f);
+            lval[warp * WCAP + j] = e;
+          }
+          __syncthreads();
+        }
+      }
+      if (oc.accept < 0) {
+        const float W = list_weights(0, 1.f);
+        oc.token = W > 0.f ? list_locate(u_final, W) : -1;
+        if (!(W > 0.f)) oc.status |= SPEC_SEQ_RESID_ZERO;
+      }
+    }
+  }
+  if (threadIdx.x >= 32) return;
+  finish_row(p, row, oc, sh);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1537,9 +2085,48 @@ spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t 
   return launch_status();
 }
 
+size_t stream_smem() {
+  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8;
+}
+
+spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(sampler_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem()) != cudaSuccess)
+      return SPEC_ECUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows, 1, 1);
+  cfg.blockDim = dim3(kSNT, 1, 1);
+  cfg.dynamicSmemBytes = stream_smem();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (its radix fallback
+  attr[0].val.clusterDim.x = 1;                        // uses the cluster exchange helpers)
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, sampler_stream_kernel, prm) != cudaSuccess) return SPEC_ECUDA;
+  return launch_status();
+}
+
 spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
   // full-vocabulary residuals (no truncation) stage q's slice in shared memory
   const bool trunc = (prm.top_k > 0 && prm.top_k < V) || (prm.top_p > 0.f && prm.top_p < 1.f);
+  // many truncated rows: one streaming CTA per row (every SM busy, no
+  // cluster exchanges); trees only when their kept set fits the lists
+  {
+    const long long ctas = (long long)B * R * cluster_size(V);
+    const bool many = ctas > 2LL * num_sms_cached();
+    if (many && trunc && !prm.greedy &&
+        (!prm.tree || (prm.top_k > 0 && prm.top_k <= kSCap / (kSNT / 32)))) {
+      prm.slice = V;
+      return launch_stream(prm, B * R, st);
+    }
+  }
   prm.qsm = (!prm.greedy && prm.qbulk && !trunc) ? 1 : 0;
   const SampPlan pl = plan_sampler(B, R, V, prm.qsm != 0);
   if ((size_t)pl.slice * 4 > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
