@@ -171,6 +171,12 @@ SPEC_DEV float texp(float l, float nm, float lfloor, float c_hi, float c_lo) {
   return __fmaf_rn(y, __fmul_rn(xl, kLn2), y);
 }
 
+// exp((l - m) / T) with one FMA and the special-function unit: nmc = -m * c_hi.
+// Used when p itself is not returned: the decisions only need p to a few
+// 1e-6 relative (the error grows with the distance below the maximum, where
+// p is tiny); the exact float-pair form above serves p_out.
+SPEC_DEV float fexp(float l, float c_hi, float nmc) { return ex2_approx(__fmaf_rn(l, c_hi, nmc)); }
+
 // Histogram bin of E in [0, 1]: bins 0..1023 hold 32 per octave, all E of a
 // bin share one exponent (126 - b/32); bin 1024 holds the rest (E < 2^-32).
 SPEC_DEV int ebin(uint32_t bits) {
@@ -313,9 +319,9 @@ SPEC_DEV void exchange(const Post& mine, int CS, int& ph, Sh<NW>& sh) {
 
 SPEC_DEV bool cut_keeps(const Cut& c, float e, int id, const float* lrow_full) {
   if (c.mode == 0) return true;
-  if (c.mode == 1) {
-    if (e > c.etau) return true;
-    if (e < c.etau) return false;
+  if (c.mode == 1) {  // E decides only well away from the cut's E (2^-20 relative)
+    if (e > c.etau * (1.0f + 9.5367431640625e-07f)) return true;
+    if (e < c.etau * (1.0f - 9.5367431640625e-07f)) return false;
   }
   return is_kept(okey(__ldg(lrow_full + id)), id, c.tau, c.tie);
 }
@@ -999,7 +1005,7 @@ SPEC_DEV void finish_row(const SP& p, int row, const Outcome& oc, Sh<NW>& sh) {
 //   tree node v: the first accepted child (residual p' updated after each
 //     rejected child) or, if none, the final token drawn from p'.
 // The cluster that finishes a sequence's last row assembles the sequence.
-template <int NT>
+template <int NT, bool FAST>
 __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   constexpr int NW = NT / 32;
   constexpr int kWL = kListPerCTA / NW;
@@ -1154,7 +1160,8 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   } else {
     // ---- 3. E in place, Z (compensated per thread), histogram, probe value
     const float nm = -m, lfloor = m - 150.f * p.T;
-    const float c_hi = p.c_hi, c_lo = p.c_lo;
+    const float c_hi = p.c_hi, c_lo = p.c_lo, nmc = -m * p.c_hi;
+    auto Eof = [&](float l) { return FAST ? fexp(l, c_hi, nmc) : texp(l, nm, lfloor, c_hi, c_lo); };
     float zs = 0.f, zc = 0.f;  // Kahan sum and compensation
     {
       const int n4 = n >> 2;
@@ -1162,10 +1169,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       for (int k4 = threadIdx.x; k4 < n4; k4 += NT) {
         const float4 v = b4[k4];
         float4 e;
-        e.x = texp(v.x, nm, lfloor, c_hi, c_lo);
-        e.y = texp(v.y, nm, lfloor, c_hi, c_lo);
-        e.z = texp(v.z, nm, lfloor, c_hi, c_lo);
-        e.w = texp(v.w, nm, lfloor, c_hi, c_lo);
+        e.x = Eof(v.x);
+        e.y = Eof(v.y);
+        e.z = Eof(v.z);
+        e.w = Eof(v.w);
         b4[k4] = e;
         const float ev[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
@@ -1183,7 +1190,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
         }
       }
       for (int k = 4 * n4 + threadIdx.x; k < n; k += NT) {
-        const float e = texp(buf[k], nm, lfloor, c_hi, c_lo);
+        const float e = Eof(buf[k]);
         buf[k] = e;
         const float y = e - zc;
         const float t = zs + y;
@@ -1436,7 +1443,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
         if (tokn == -2) {  // residual with zero mass (rounding only): draw from p
           oc.status |= SPEC_SEQ_RESID_ZERO;
           for (int k = it.r0 + lane; k < it.r1; k += 32)
-            buf[k] = texp(__ldg(lrow + k), nm, lfloor, c_hi, c_lo);
+            buf[k] = Eof(__ldg(lrow + k));
           __syncthreads();
           it.listed = false;
           const float t2 = weight_full<NT>(buf, it.r0, it.r1, cut, lo, lrow_full, 0, 1.f, qlo,
@@ -1485,7 +1492,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
           const int cnt = it.count(sh);
           for (int j = lane; j < cnt; j += 32) {
             const int k = it.at(j);
-            float e = texp(__ldg(lrow + k), nm, lfloor, c_hi, c_lo);
+            float e = Eof(__ldg(lrow + k));
             e = cut_keeps(cut, e, lo + k, lrow_full) ? e : 0.f;
             for (int s = 0; s < nsteps; ++s)
               e = residual_w(e, sh.invw_used[s],
@@ -1531,6 +1538,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 constexpr int kSNT = 1024;
 constexpr int kSCap = 16384;  // kept positions listed per row (kSCap / 32 per warp)
 
+template <bool FAST>
 __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   constexpr int NT = kSNT, NW = NT / 32, WCAP = kSCap / NW;
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -1629,7 +1637,8 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // ---- 2. Z (E recomputed, compensated per thread), histogram, probe value
     const float nm = -m, lfloor = m - 150.f * p.T;
     const float c_hi = p.c_hi, c_lo = p.c_lo;
-    auto Eof = [&](float l) { return texp(l, nm, lfloor, c_hi, c_lo); };
+    const float nmc = -m * c_hi;
+    auto Eof = [&](float l) { return FAST ? fexp(l, c_hi, nmc) : texp(l, nm, lfloor, c_hi, c_lo); };
     float zs = 0.f, zc = 0.f;
     auto visit2 = [&](int k, float l) {
       const float e = Eof(l);
@@ -2060,11 +2069,11 @@ size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
   return off;
 }
 
-template <int NT>
+template <int NT, bool FAST>
 spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t st) {
   static bool attr_set = false;  // once, at the largest size, so graph captures need no setup
   if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sampler_kernel<NT, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_smem(kMaxSliceBytes, true)) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
@@ -2081,7 +2090,7 @@ spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sampler_kernel<NT>, prm) != cudaSuccess) return SPEC_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sampler_kernel<NT, FAST>, prm) != cudaSuccess) return SPEC_ECUDA;
   return launch_status();
 }
 
@@ -2089,10 +2098,11 @@ size_t stream_smem() {
   return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8;
 }
 
+template <bool FAST>
 spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sampler_stream_kernel<FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)stream_smem()) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
@@ -2109,7 +2119,7 @@ spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sampler_stream_kernel, prm) != cudaSuccess) return SPEC_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sampler_stream_kernel<FAST>, prm) != cudaSuccess) return SPEC_ECUDA;
   return launch_status();
 }
 
@@ -2124,14 +2134,18 @@ spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
     if (many && trunc && !prm.greedy &&
         (!prm.tree || (prm.top_k > 0 && prm.top_k <= kSCap / (kSNT / 32)))) {
       prm.slice = V;
-      return launch_stream(prm, B * R, st);
+      return prm.p_out ? launch_stream<false>(prm, B * R, st) : launch_stream<true>(prm, B * R, st);
     }
   }
   prm.qsm = (!prm.greedy && prm.qbulk && !trunc) ? 1 : 0;
   const SampPlan pl = plan_sampler(B, R, V, prm.qsm != 0);
   if ((size_t)pl.slice * 4 > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
   prm.slice = pl.slice;
-  return pl.NT == 512 ? launch_nt<512>(prm, pl, B * R, st) : launch_nt<256>(prm, pl, B * R, st);
+  if (prm.p_out)
+    return pl.NT == 512 ? launch_nt<512, false>(prm, pl, B * R, st)
+                        : launch_nt<256, false>(prm, pl, B * R, st);
+  return pl.NT == 512 ? launch_nt<512, true>(prm, pl, B * R, st)
+                      : launch_nt<256, true>(prm, pl, B * R, st);
 }
 
 spec_status check_cfg(const spec_sampler* cfg) {

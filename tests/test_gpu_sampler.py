@@ -143,13 +143,18 @@ SMALL = [
 @pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
 @pytest.mark.parametrize("V", [1000, 4099, 40000])
 def test_small_batches(name, kw, V):
-    spec = wl.Spec(name, B=48, Hq=1, Hkv=1, D=64, V=V, ctx=(1, 1), gamma=7, logit_sd=3.0,
-                   draft_div=kw.get("temperature", 1.0), draft_noise=0.8, **kw)
-    nflag = 0
-    for seed in range(2):
-        w, gpu, ref = chain_case(spec, 10 * seed + V % 7)
-        nflag += compare(gpu, ref)
-        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+    # B=48: the many-row path for truncated configs; B=3: the cluster path.
+    # With p requested the exact exp is used; without it, the fast one.
+    for B in (48, 3):
+        spec = wl.Spec(name, B=B, Hq=1, Hkv=1, D=64, V=V, ctx=(1, 1), gamma=7, logit_sd=3.0,
+                       draft_div=kw.get("temperature", 1.0), draft_noise=0.8, **kw)
+        for seed in range(2):
+            w, gpu, ref = chain_case(spec, 10 * seed + V % 7)
+            compare(gpu, ref)
+            check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+            gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
+                             want_p=False)
+            compare(gpu2, ref)
 
 
 def test_greedy_small_and_ties():
@@ -236,14 +241,22 @@ def test_full_vocab_chain(name):
         flagged += compare(gpu, ref)
         if not greedy:
             check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+            gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
+                             want_p=False)
+            compare(gpu2, ref)
 
 
 def test_batched_serving_topp_sample():
+    # B=8 (40 rows x 8-CTA clusters: the many-row path) and B=2 (the cluster path)
     for name in ("batched_serving_a45", "batched_serving_a75"):
-        spec = wl.SPECS[name].with_(B=8)
-        w, gpu, ref = chain_case(spec, 3)
-        compare(gpu, ref)
-        check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+        for B in (8, 2):
+            spec = wl.SPECS[name].with_(B=B)
+            w, gpu, ref = chain_case(spec, 3)
+            compare(gpu, ref)
+            check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+            gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
+                             want_p=False)
+            compare(gpu2, ref)
 
 
 # ------------------------------------------------------------------ tree
@@ -266,6 +279,9 @@ def test_tree_small(top_k):
         w, gpu, ref = tree_case(spec, seed)
         compare(gpu, ref, tree=True)
         check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+        gpu2 = run_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms,
+                        cfg_of(spec), want_p=False)
+        compare(gpu2, ref, tree=True)
     w, gpu, ref = tree_case(spec, 7, greedy=True)
     compare(gpu, ref, tree=True)
 
@@ -275,6 +291,9 @@ def test_tree_draft_tree_config():
     w, gpu, ref = tree_case(spec, spec.seed)
     compare(gpu, ref, tree=True)
     check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+    gpu2 = run_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms, cfg_of(spec),
+                    want_p=False)
+    compare(gpu2, ref, tree=True)
 
 
 def test_tree_first_token_follows_p_root_on_gpu():
