@@ -293,18 +293,10 @@ def bench_gpu(args, spec, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": spec.name, "global_batch": spec.B * ws, "seq_len": int(ctx.max()),
-            "rows_per_seq": spec.R, "tree": spec.is_tree, "q_heads": spec.Hq,
-            "kv_heads": spec.Hkv, "head_dim": spec.D, "vocab": spec.V, "page_size": spec.page_size,
-            "temperature": spec.temperature, "top_k": spec.top_k, "top_p": spec.top_p,
-            "greedy": spec.greedy, "num_splits": step.sv.attn_num_splits(
-                spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
-                step.w.block_table.shape[1], spec.num_splits),
-            "sampler_dtype": "f32", "parallelism": f"replicas{ws}",
-            "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read of a second "
-                  "buffer; outside the timed events)",
-            "timing": "CUDA-graph replay, CUDA events per step"},
+        "config": arm_config(spec, int(ctx.max()), ws),
+        "attn_num_splits": step.sv.attn_num_splits(
+            spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
+            step.w.block_table.shape[1], spec.num_splits),
         "sequences_per_s": sum_over_ranks(spec.B, ws, device=dev) / (mean_ms_all * 1e-3),
         "step_hbm_gbs": step_gbs, "step_hbm_frac": step_gbs / peak,
         "step_algorithmic_bytes": nbytes["step"],
@@ -320,6 +312,19 @@ def bench_gpu(args, spec, ws, rank, local):
         "clocks": clocks,
     }
     return out
+
+
+def arm_config(spec, seq_len, ws):
+    """The workload description both arms print (identical keys and values)."""
+    return {
+        "workload": spec.name, "global_batch": spec.B * ws, "seq_len": seq_len,
+        "rows_per_seq": spec.R, "tree": spec.is_tree, "q_heads": spec.Hq,
+        "kv_heads": spec.Hkv, "head_dim": spec.D, "vocab": spec.V, "page_size": spec.page_size,
+        "temperature": spec.temperature, "top_k": spec.top_k, "top_p": spec.top_p,
+        "greedy": spec.greedy, "parallelism": f"replicas{ws}",
+        "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read of a second "
+              "buffer; outside the timed events)",
+        "timing": "CUDA-graph replay, CUDA events per step"}
 
 
 def bench_e2e(step: GpuStep, spec, n, ws, dev):
@@ -436,7 +441,8 @@ def bench_reference(args, spec):
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "impl": "reference", "config": {"workload": spec.name, "global_batch": spec.B},
+            "impl": "reference",
+            "config": arm_config(spec, int(np.asarray(w.ctx_len).max()), 1),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
