@@ -144,6 +144,26 @@ SPEC_DEV bool is_kept(uint32_t key, int id, uint32_t tau, int tie) {
   return key > tau || (key == tau && id <= tie);
 }
 
+// global loads that ask L2 to keep the line (the row is swept several times):
+// an L2 cache policy with evict-last priority
+SPEC_DEV uint64_t l2_keep_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+SPEC_DEV float4 ldg_keep4(const float4* p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+SPEC_DEV float ldg_keep(const float* p, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
 SPEC_DEV float fmax_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
@@ -175,18 +195,22 @@ SPEC_DEV float texp(float l, float nm, float lfloor, float c_hi, float c_lo) {
 // Used when p itself is not returned: the decisions only need p to a few
 // 1e-6 relative (the error grows with the distance below the maximum, where
 // p is tiny); the exact float-pair form above serves p_out.
-SPEC_DEV float fexp(float l, float c_hi, float nmc) { return ex2_approx(__fmaf_rn(l, c_hi, nmc)); }
+SPEC_DEV float fexp(float l, float c_hi, float nmc) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(__fmaf_rn(l, c_hi, nmc)));
+  return y;  // results below 2^-126 flush to 0: such p cannot decide anything
+}
 
 // Histogram bin of E in [0, 1]: bins 0..1023 hold 32 per octave, all E of a
 // bin share one exponent (126 - b/32); bin 1024 holds the rest (E < 2^-32).
 SPEC_DEV int ebin(uint32_t bits) {
-  const int d = 0x3F7FFFFF - (int)bits;
-  return d < 0 ? 0 : min(d >> 18, kBins);
+  return min((0x3F7FFFFF - (int)min(bits, 0x3F7FFFFFu)) >> 18, kBins);  // E >= 1: bin 0
 }
 
 // E rounded to a 16-bit significand, in units of 2^(-16 - b/32) of its bin b
 SPEC_DEV uint32_t m16(uint32_t bits) {
-  return bits >= 0x3F800000u ? 65536u : ((((bits & 0x7FFFFFu) | 0x800000u) + 128u) >> 8);
+  // E >= 1 clamps to the largest significand below 1, which rounds to 65536 = 1.0
+  return ((((min(bits, 0x3F7FFFFFu) & 0x7FFFFFu) | 0x800000u) + 128u) >> 8);
 }
 
 // a bin's sum of m16 in units of 2^-44
@@ -1564,6 +1588,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   const bool vec = p.bulk != 0;  // V % 4 == 0 and 16-byte aligned rows
   const int n4 = vec ? V / 4 : 0;
   const float4* l4 = reinterpret_cast<const float4*>(lrow);
+  const uint64_t pol = l2_keep_policy();
   // every element of the row once: visit(k, l), four 16-byte loads in flight per thread
   auto sweep = [&](auto&& visit) {
     for (int base = threadIdx.x; base < n4; base += 4 * NT) {
@@ -1571,7 +1596,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int k4 = base + u * NT;
-        v[u] = k4 < n4 ? __ldg(l4 + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = k4 < n4 ? ldg_keep4(l4 + k4, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -1584,7 +1609,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
       }
     }
-    for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) visit(k, __ldg(lrow + k));
+    for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) visit(k, ldg_keep(lrow + k, pol));
   };
   int ph = 0;
 
@@ -1640,21 +1665,46 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     const float nmc = -m * c_hi;
     auto Eof = [&](float l) { return FAST ? fexp(l, c_hi, nmc) : texp(l, nm, lfloor, c_hi, c_lo); };
     float zs = 0.f, zc = 0.f;
-    auto visit2 = [&](int k, float l) {
-      const float e = Eof(l);
-      const float y = e - zc;
+    auto kahan = [&](float x) {
+      const float y = x - zc;
       const float t = zs + y;
       zc = (t - zs) - y;
       zs = t;
-      if (k == probe) sh.eprobe = e;
+    };
+    auto hist = [&](float e) {
+      const uint32_t bits = __float_as_uint(e);
+      const int bn = ebin(bits);
+      if (topk) atomicAdd(&hcnt[bn], 1u);
+      if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+    };
+    // four elements: their E, a pairwise partial sum into the compensated sum
+    auto visit4 = [&](float4 l) {
+      const float e0 = Eof(l.x), e1 = Eof(l.y), e2 = Eof(l.z), e3 = Eof(l.w);
+      kahan((e0 + e1) + (e2 + e3));
       if (trunc) {
-        const uint32_t bits = __float_as_uint(e);
-        const int bn = ebin(bits);
-        if (topk) atomicAdd(&hcnt[bn], 1u);
-        if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+        hist(e0);
+        hist(e1);
+        hist(e2);
+        hist(e3);
       }
     };
-    sweep(visit2);
+    for (int base = threadIdx.x; base < n4; base += 4 * NT) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k4 = base + u * NT;
+        v[u] = k4 < n4 ? ldg_keep4(l4 + k4, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (base + u * NT < n4) visit4(v[u]);
+    }
+    for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) {
+      const float e = Eof(ldg_keep(lrow + k, pol));
+      kahan(e);
+      if (trunc) hist(e);
+    }
+    if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(__ldg(lrow + probe));
     const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
     const float zl = block_sum_f<NT>(-zc, sh);
     const float e_probe = sh.eprobe;
@@ -1662,6 +1712,10 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 
     Cut cut{0, 0.f, 0u, INT_MAX};
     float zkept = zh + zl;
+    // each warp owns one contiguous id range of the row (multiple of 4 long)
+    const int rw = ((V + NW - 1) / NW + 3) / 4 * 4;
+    const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
+    bool cand_lists = false;  // lists hold every element that can be kept (ids, logits)
     if (trunc) {
       // ---- 3. the cut: bin range, members, selection (or the radix fallback)
       if (warp == 0) {
@@ -1696,8 +1750,8 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         const uint32_t edge = (uint32_t)(0x3F7FFFFF - ((b_hi + 1) << 18) + 1);
         const float lpre = m + p.T * (__logf(__uint_as_float(edge)) - 1e-3f);
         unsigned long long above = 0;
-        auto visit3 = [&](int k, float l) {
-          if (!(l >= lpre)) return;
+        // an element that passed the pre-filter: above the range, a member, or below
+        auto consider = [&](int k, float l) {
           const uint32_t bits = __float_as_uint(Eof(l));
           if (bits < edge) return;
           const int bn = ebin(bits);
@@ -1711,7 +1765,61 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
             }
           }
         };
-        sweep(visit3);
+        // the pre-filter's survivors of each warp's range, compacted in id order into
+        // the warp's list (id, logit); they include every element the cut can keep
+        int cntw = 0;
+        for (int s0 = r0; s0 < r1; s0 += 512) {
+          float lv[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int k = s0 + 128 * u + 4 * lane;
+            if (vec && k + 3 < r1) {
+              const float4 v = ldg_keep4(reinterpret_cast<const float4*>(lrow + k), pol);
+              lv[u][0] = v.x;
+              lv[u][1] = v.y;
+              lv[u][2] = v.z;
+              lv[u][3] = v.w;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                lv[u][j] = k + j < r1 ? ldg_keep(lrow + k + j, pol) : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int k = s0 + 128 * u + 4 * lane;
+            int c = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c += lv[u][j] >= lpre ? 1 : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int t = __shfl_up_sync(kFull, incl, o);
+              if (lane >= o) incl += t;
+            }
+            int pos = cntw + incl - c;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (lv[u][j] >= lpre) {
+                if (pos < WCAP) {
+                  lid[warp * WCAP + pos] = k + j;
+                  lval[warp * WCAP + pos] = lv[u][j];
+                }
+                ++pos;
+              }
+            cntw += __shfl_sync(kFull, incl, 31);
+          }
+        }
+        if (lane == 0) sh.list_n[warp] = cntw;
+        cand_lists = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
+        if (cand_lists) {
+          for (int j = lane; j < cntw; j += 32)
+            consider(lid[warp * WCAP + j], lval[warp * WCAP + j]);
+        } else {
+          sweep([&](int k, float l) {
+            if (l >= lpre) consider(k, l);
+          });
+        }
         const unsigned long long a_lo = block_sum_u64<NT>(above, sh);  // barriers: members complete
         const int total = sh.bi[4];
         if (total > NT || total < 1) {
@@ -1726,6 +1834,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
       }
       if (tmode == 2) {
+        cand_lists = false;
         cut = cut_radix<NT>(p, lrow, [&](int k) { return Eof(__ldg(lrow + k)); }, V, 0, rs, 0, 1,
                             ph, sh);
         float s = 0.f, cmp = 0.f;
@@ -1748,22 +1857,42 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     auto kept_l = [&](float l, int id) { return !trunc || is_kept(okey(l), id, cut.tau, cut.tie); };
 
     // ---- 4. (on first use) list each warp's kept positions with their E
-    const int rw = ((V + NW - 1) / NW + 3) / 4 * 4;
-    const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
     bool listed = false, list_ready = false;
     auto ensure_list = [&]() {
       if (list_ready) return;
       list_ready = true;
+      if (cand_lists) {
+        // keep the candidates the cut keeps (in place, order preserved), logit -> E
+        const int cnt = sh.list_n[warp];
+        int kept = 0;
+        for (int s0 = 0; s0 < cnt; s0 += 32) {
+          const int j = s0 + lane;
+          const int id = j < cnt ? lid[warp * WCAP + j] : 0;
+          const float l = j < cnt ? lval[warp * WCAP + j] : 0.f;
+          const bool kp = j < cnt && kept_l(l, id);
+          const unsigned bal = __ballot_sync(kFull, kp);
+          if (kp) {
+            const int pos = kept + __popc(bal & ((1u << lane) - 1));
+            lid[warp * WCAP + pos] = id;
+            lval[warp * WCAP + pos] = Eof(l);
+          }
+          kept += __popc(bal);
+        }
+        __syncwarp();
+        if (lane == 0) sh.list_n[warp] = kept;
+        listed = true;
+        __syncthreads();
+      } else {
       int cntw = 0;
-      for (int s0 = r0; s0 < r1; s0 += 128) {
-        float lv[4];
+      for (int s0 = r0; s0 < r1; s0 += 512) {
+        float lv[16];  // sixteen loads in flight per lane
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int k = s0 + 32 * u + lane;
-          lv[u] = k < r1 ? __ldg(lrow + k) : 0.f;
+          lv[u] = k < r1 ? ldg_keep(lrow + k, pol) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int k = s0 + 32 * u + lane;
           const bool kp = k < r1 && kept_l(lv[u], k);
           const unsigned bal = __ballot_sync(kFull, kp);
@@ -1777,6 +1906,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       }
       if (lane == 0) sh.list_n[warp] = cntw;
       listed = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
+      }
       // list positions of the node's children (binary search in the owning warp's list)
       if (listed && p.tree)
         for (int c = threadIdx.x; c < R; c += NT) {
