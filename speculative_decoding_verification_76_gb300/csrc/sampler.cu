@@ -1560,7 +1560,9 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 // E) is then listed per warp in shared memory for the draws and the tree's
 // residuals.  No cluster exchanges: every SM works on its own rows.
 constexpr int kSNT = 1024;
-constexpr int kSCap = 16384;  // kept positions listed per row (kSCap / 32 per warp)
+constexpr int kSCap = 16384;    // list entries per row (kSCap / 32 per warp)
+constexpr int kSBudget = 10240; // candidates a row's floor aims at (sampled estimate)
+constexpr int kSWords = 8192;   // flag words: rows of up to 32 * kSWords ids are listed
 
 template <bool FAST>
 __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
@@ -1572,6 +1574,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   uint32_t* xbits = reinterpret_cast<uint32_t*>(xkey + NT);                          // NT
   int* lid = reinterpret_cast<int*>(xbits + NT);                                      // kSCap
   float* lval = reinterpret_cast<float*>(lid + kSCap);                                // kSCap
+  uint32_t* fbits = reinterpret_cast<uint32_t*>(lval + kSCap);                        // kSWords
   const RadixScratch rs{reinterpret_cast<uint32_t*>(xkey), xkey + 256, xkey + 768,
                         reinterpret_cast<uint32_t*>(xkey) + 2048};
   __shared__ Sh<NW> sh;
@@ -1645,7 +1648,27 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       qrow = p.q + ((size_t)b * (R - 1) + i) * V;
   }
 
-  // ---- 1. maximum (NaN-propagating)
+  // each warp owns one contiguous id range of the row (a multiple of 32 long);
+  // four logits of ids k..k+3 at a time (-inf past the range)
+  const int rw = ((V + NW - 1) / NW + 31) / 32 * 32;
+  const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
+  auto load4 = [&](int k, float (&lv)[4]) {
+    if (vec && k + 3 < r1) {
+      const float4 v = ldg_keep4(reinterpret_cast<const float4*>(lrow + k), pol);
+      lv[0] = v.x;
+      lv[1] = v.y;
+      lv[2] = v.z;
+      lv[3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lv[j] = k + j < r1 ? ldg_keep(lrow + k + j, pol) : -INFINITY;
+    }
+  };
+  const unsigned lt = (1u << lane) - 1u;
+
+  // ---- 1. maximum (NaN-propagating); one sample per thread, evenly spaced
+  // over the row, for the candidate floor
+  const float smp = trunc ? ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol) : 0.f;
   float mx = -INFINITY;
   sweep([&](int, float l) { mx = fmax_nan(mx, l); });
 #pragma unroll
@@ -1659,11 +1682,45 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   Outcome oc{0, -1, 0, bad ? 1 : 0};
 
   if (!bad) {
-    // ---- 2. Z (E recomputed, compensated per thread), histogram, probe value
     const float nm = -m, lfloor = m - 150.f * p.T;
     const float c_hi = p.c_hi, c_lo = p.c_lo;
     const float nmc = -m * c_hi;
     auto Eof = [&](float l) { return FAST ? fexp(l, c_hi, nmc) : texp(l, nm, lfloor, c_hi, c_lo); };
+    auto hist = [&](uint32_t bits, int bn) {
+      if (topk) atomicAdd(&hcnt[bn], 1u);
+      if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
+    };
+    auto hist_e = [&](float e) {
+      const uint32_t bits = __float_as_uint(e);
+      hist(bits, ebin(bits));
+    };
+
+    // ---- 2. the candidate floor (truncated rows): the deepest E bin whose
+    // sampled count at or above it stays within the list budget; the elements
+    // of bins <= bf are listed.  -1: no floor (every element histogrammed)
+    int bf = -1;
+    if (trunc && V <= 32 * kSWords) {
+      const float budget =
+          topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
+      const int ns = (int)(budget * (float)NT / (float)V);
+      if (ns >= 1 && (!topk || p.top_k <= kSBudget / 2)) {
+        const int sbin = ebin(__float_as_uint(Eof(smp)));
+        int lo = -1, hi = kBins - 1;  // the largest b with count(sample bin <= b) <= ns
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (__syncthreads_count(sbin <= mid) <= ns) lo = mid; else hi = mid - 1;
+        }
+        bf = lo;
+      }
+    }
+    const bool listing = bf >= 0;
+    // E bits at or above edge_f <=> bin <= bf
+    const uint32_t edge_f = listing ? (uint32_t)(0x3F7FFFFF - ((bf + 1) << 18) + 1) : 0xFFFFFFFFu;
+
+    // ---- 3. Z (E recomputed, compensated per thread; four at a time); with a
+    // floor, one bit per id for the elements at or above it, else the
+    // histogram of every element
+    const bool zhist = trunc && !listing;
     float zs = 0.f, zc = 0.f;
     auto kahan = [&](float x) {
       const float y = x - zc;
@@ -1671,40 +1728,106 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       zc = (t - zs) - y;
       zs = t;
     };
-    auto hist = [&](float e) {
-      const uint32_t bits = __float_as_uint(e);
-      const int bn = ebin(bits);
-      if (topk) atomicAdd(&hcnt[bn], 1u);
-      if (topp && bn < kBins) atomicAdd(&hm[bn], m16(bits));
-    };
-    // four elements: their E, a pairwise partial sum into the compensated sum
-    auto visit4 = [&](float4 l) {
-      const float e0 = Eof(l.x), e1 = Eof(l.y), e2 = Eof(l.z), e3 = Eof(l.w);
-      kahan((e0 + e1) + (e2 + e3));
-      if (trunc) {
-        hist(e0);
-        hist(e1);
-        hist(e2);
-        hist(e3);
-      }
-    };
-    for (int base = threadIdx.x; base < n4; base += 4 * NT) {
+    for (int b0 = 0; b0 < n4; b0 += 4 * NT) {  // warp-uniform trip count
       float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int k4 = base + u * NT;
-        v[u] = k4 < n4 ? ldg_keep4(l4 + k4, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int k4 = b0 + u * NT + threadIdx.x;
+        v[u] = k4 < n4 ? ldg_keep4(l4 + k4, pol) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (base + u * NT < n4) visit4(v[u]);
+      for (int u = 0; u < 4; ++u) {
+        const int k4 = b0 + u * NT + threadIdx.x;
+        const float e0 = Eof(v[u].x), e1 = Eof(v[u].y), e2 = Eof(v[u].z), e3 = Eof(v[u].w);
+        kahan((e0 + e1) + (e2 + e3));
+        if (zhist && k4 < n4) {
+          hist_e(e0);
+          hist_e(e1);
+          hist_e(e2);
+          hist_e(e3);
+        }
+        if (listing) {
+          // ids 4 k4 .. 4 k4 + 3; eight lanes make one word of 32 ids
+          uint32_t nib = (__float_as_uint(e0) >= edge_f ? 1u : 0u) |
+                         (__float_as_uint(e1) >= edge_f ? 2u : 0u) |
+                         (__float_as_uint(e2) >= edge_f ? 4u : 0u) |
+                         (__float_as_uint(e3) >= edge_f ? 8u : 0u);
+          if (k4 >= n4) nib = 0u;
+          nib <<= 4 * (lane & 7);
+          nib |= __shfl_xor_sync(kFull, nib, 1);
+          nib |= __shfl_xor_sync(kFull, nib, 2);
+          nib |= __shfl_xor_sync(kFull, nib, 4);
+          if ((lane & 7) == 0 && k4 < n4) fbits[k4 >> 3] = nib;
+        }
+      }
     }
-    for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) {
-      const float e = Eof(ldg_keep(lrow + k, pol));
+    // rows without 16-byte vectors: one id per thread, one word per warp
+    for (int k0 = 4 * n4; k0 < V; k0 += NT) {
+      const int k = k0 + threadIdx.x;
+      const float e = k < V ? Eof(ldg_keep(lrow + k, pol)) : 0.f;
       kahan(e);
-      if (trunc) hist(e);
+      if (zhist && k < V) hist_e(e);
+      if (listing) {
+        const unsigned word = __ballot_sync(kFull, k < V && __float_as_uint(e) >= edge_f);
+        if (lane == 0 && k < V) fbits[k >> 5] = word;
+      }
     }
     if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(__ldg(lrow + probe));
+
+    // ---- 4. the candidate lists: each warp lists the flagged ids of its
+    // range in id order, then their logits; the histogram of the listed
+    // elements (they are exactly those of bins <= bf)
+    int cntw = 0;
+    if (listing) {
+      __syncthreads();  // flag words complete
+      const int w0 = (r0 + 31) >> 5, w1 = (r1 + 31) >> 5;  // r0: a multiple of 32, or V
+      for (int wb = w0; wb < w1; wb += 32) {
+        const int wd = wb + lane;
+        uint32_t word = wd < w1 ? fbits[wd] : 0u;
+        const int c = __popc(word);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t;
+        }
+        int pos = cntw + incl - c;
+        while (word) {
+          const int bpos = __ffs(word) - 1;
+          word &= word - 1u;
+          if (pos < WCAP) lid[warp * WCAP + pos] = 32 * wd + bpos;
+          ++pos;
+        }
+        cntw += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) sh.list_n[warp] = cntw;
+    }
+    const bool fit = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
+    // lists hold every element that can be kept (ids, logits)
+    bool cand_lists = listing && fit;
+    if (cand_lists) {
+      const int cnt = cntw;
+      for (int j0 = 0; j0 < cnt; j0 += 32 * 8) {
+        float lvv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + 32 * u + lane;
+          lvv[u] = j < cnt ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + 32 * u + lane;
+          if (j < cnt) {
+            lval[warp * WCAP + j] = lvv[u];
+            hist_e(Eof(lvv[u]));
+          }
+        }
+      }
+    } else if (listing) {
+      // a list overflowed: the histogram of every element
+      sweep([&](int, float l) { hist_e(Eof(l)); });
+      bf = -1;
+    }
     const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
     const float zl = block_sum_f<NT>(-zc, sh);
     const float e_probe = sh.eprobe;
@@ -1712,37 +1835,49 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 
     Cut cut{0, 0.f, 0u, INT_MAX};
     float zkept = zh + zl;
-    // each warp owns one contiguous id range of the row (multiple of 4 long)
-    const int rw = ((V + NW - 1) / NW + 3) / 4 * 4;
-    const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
-    bool cand_lists = false;  // lists hold every element that can be kept (ids, logits)
     if (trunc) {
-      // ---- 3. the cut: bin range, members, selection (or the radix fallback)
-      if (warp == 0) {
-        int mode, bl, bh, kx;
-        find_range<NT>(
-            topk, topp, p.top_k, p.top_p, zall,
-            [&](int o, unsigned long long& c, unsigned long long& mm) {
-              for (int j = 0; j < 32; ++j) {
-                if (topk) c += hcnt[32 * o + j];
-                if (topp) mm += hm[32 * o + j];
-              }
-            },
-            [&](int bb, unsigned long long& c, unsigned long long& mm) {
-              if (topk) c += hcnt[bb];
-              if (topp) mm += hm[bb];
-            },
-            &mode, &bl, &bh, &kx);
-        if (lane == 0) {
-          sh.bi[0] = mode;
-          sh.bi[1] = bl;
-          sh.bi[2] = bh;
-          sh.bi[3] = kx;
-          sh.bi[4] = 0;
+      // ---- 5. the cut: bin range, members, selection (or the radix fallback)
+      auto run_find = [&]() {
+        if (warp == 0) {
+          int mode, bl, bh, kx;
+          find_range<NT>(
+              topk, topp, p.top_k, p.top_p, zall,
+              [&](int o, unsigned long long& c, unsigned long long& mm) {
+                for (int j = 0; j < 32; ++j) {
+                  const int bb = 32 * o + ((j + o) & 31);  // lanes start at different banks
+                  if (topk) c += hcnt[bb];
+                  if (topp) mm += hm[bb];
+                }
+              },
+              [&](int bb, unsigned long long& c, unsigned long long& mm) {
+                if (topk) c += hcnt[bb];
+                if (topp) mm += hm[bb];
+              },
+              &mode, &bl, &bh, &kx);
+          if (lane == 0) {
+            sh.bi[0] = mode;
+            sh.bi[1] = bl;
+            sh.bi[2] = bh;
+            sh.bi[3] = kx;
+            sh.bi[4] = 0;
+          }
         }
-      }
-      __syncthreads();
+        __syncthreads();
+      };
+      run_find();
       int tmode = sh.bi[0];
+      if (tmode == 2 && cand_lists) {
+        // the cut lies below the listed bins: histogram the rest, search again
+        sweep([&](int, float l) {
+          const uint32_t bits = __float_as_uint(Eof(l));
+          const int bn = ebin(bits);
+          if (bn > bf) hist(bits, bn);
+        });
+        __syncthreads();
+        run_find();
+        tmode = sh.bi[0];
+        cand_lists = false;
+      }
       const int b_lo = sh.bi[1], b_hi = sh.bi[2], kidx = sh.bi[3];
       if (tmode == 1) {
         // members of bins [b_lo, b_hi] and the exact mass above them; a logit
@@ -1765,55 +1900,45 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
             }
           }
         };
-        // the pre-filter's survivors of each warp's range, compacted in id order into
-        // the warp's list (id, logit); they include every element the cut can keep
-        int cntw = 0;
-        for (int s0 = r0; s0 < r1; s0 += 512) {
-          float lv[4][4];
+        if (!cand_lists) {
+          // the pre-filter's survivors of each warp's range, compacted in id order
+          // into the warp's list (id, logit); they include every element the cut
+          // can keep
+          int cw = 0;
+          for (int s0 = r0; s0 < r1; s0 += 512) {
+            float lv[4][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int k = s0 + 128 * u + 4 * lane;
-            if (vec && k + 3 < r1) {
-              const float4 v = ldg_keep4(reinterpret_cast<const float4*>(lrow + k), pol);
-              lv[u][0] = v.x;
-              lv[u][1] = v.y;
-              lv[u][2] = v.z;
-              lv[u][3] = v.w;
-            } else {
+            for (int u = 0; u < 4; ++u) load4(s0 + 128 * u + 4 * lane, lv[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k = s0 + 128 * u + 4 * lane;
+              bool f[4];
+              unsigned bal[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                f[j] = lv[u][j] >= lpre;
+                bal[j] = __ballot_sync(kFull, f[j]);
+              }
+              int pos = cw + __popc(bal[0] & lt) + __popc(bal[1] & lt) + __popc(bal[2] & lt) +
+                        __popc(bal[3] & lt);
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                lv[u][j] = k + j < r1 ? ldg_keep(lrow + k + j, pol) : -INFINITY;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int k = s0 + 128 * u + 4 * lane;
-            int c = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) c += lv[u][j] >= lpre ? 1 : 0;
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int t = __shfl_up_sync(kFull, incl, o);
-              if (lane >= o) incl += t;
-            }
-            int pos = cntw + incl - c;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (lv[u][j] >= lpre) {
-                if (pos < WCAP) {
-                  lid[warp * WCAP + pos] = k + j;
-                  lval[warp * WCAP + pos] = lv[u][j];
+                if (f[j]) {
+                  if (pos < WCAP) {
+                    lid[warp * WCAP + pos] = k + j;
+                    lval[warp * WCAP + pos] = lv[u][j];
+                  }
+                  ++pos;
                 }
-                ++pos;
-              }
-            cntw += __shfl_sync(kFull, incl, 31);
+              cw += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
+            }
           }
+          if (lane == 0) sh.list_n[warp] = cw;
+          cand_lists = __syncthreads_and(cw <= WCAP ? 1 : 0) != 0;
         }
-        if (lane == 0) sh.list_n[warp] = cntw;
-        cand_lists = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
         if (cand_lists) {
-          for (int j = lane; j < cntw; j += 32)
+          const int cnt = sh.list_n[warp];
+          for (int j = lane; j < cnt; j += 32)
             consider(lid[warp * WCAP + j], lval[warp * WCAP + j]);
         } else {
           sweep([&](int k, float l) {
@@ -1856,7 +1981,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     const float invz = 1.0f / zkept;
     auto kept_l = [&](float l, int id) { return !trunc || is_kept(okey(l), id, cut.tau, cut.tie); };
 
-    // ---- 4. (on first use) list each warp's kept positions with their E
+    // ---- 6. (on first use) list each warp's kept positions with their E
     bool listed = false, list_ready = false;
     auto ensure_list = [&]() {
       if (list_ready) return;
@@ -2078,7 +2203,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 
     const float u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
     if (!p.tree) {
-      // ---- 5a. chain: the row's test, then its correction or bonus draw
+      // ---- 7a. chain: the row's test, then its correction or bonus draw
       bool resid = false;
       if (i < R - 1) {
         const int x = probe;
@@ -2105,7 +2230,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         oc.token = tokn;
       }
     } else {
-      // ---- 5b. tree node: children in storage order against the running p'
+      // ---- 7b. tree node: children in storage order against the running p'
       ensure_list();  // the host routes here only trees whose kept set fits the lists
       oc.accept = -1;
       float invw = invz;
@@ -2225,7 +2350,7 @@ spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t 
 }
 
 size_t stream_smem() {
-  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8;
+  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8 + (size_t)kSWords * 4;
 }
 
 template <bool FAST>

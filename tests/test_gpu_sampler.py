@@ -141,7 +141,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
-@pytest.mark.parametrize("V", [1000, 4099, 40000])
+@pytest.mark.parametrize("V", [1000, 4099, 4100, 40000])
 def test_small_batches(name, kw, V):
     # B=48: the many-row path for truncated configs; B=3: the cluster path.
     # With p requested the exact exp is used; without it, the fast one.
@@ -257,6 +257,37 @@ def test_batched_serving_topp_sample():
             gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
                              want_p=False)
             compare(gpu2, ref)
+
+
+STREAM_SHAPES = [
+    # the sampled floor lies above the top-p cut (nearly flat row): the
+    # histogram is completed and the cut found again; every token is lighter
+    # than the flag margin, so p and the kept set carry the comparison
+    ("flat_topp", dict(temperature=1.0, top_p=0.9), 0.3, None),
+    # large top-k: the floor aims at the list budget
+    ("topk_3000", dict(temperature=1.0, top_k=3000), 3.0, None),
+    # 3000 high logits at the start of the row: one warp's list overflows
+    ("clustered_topp", dict(temperature=1.0, top_p=0.9), 3.0, 3000),
+]
+
+
+@pytest.mark.parametrize("name,kw,sd,clustered", STREAM_SHAPES, ids=[s[0] for s in STREAM_SHAPES])
+def test_many_rows_floor_fallbacks(name, kw, sd, clustered):
+    # 8 x 5 rows of a 152064-token vocabulary: the one-CTA-per-row path
+    spec = wl.Spec(name, B=8, Hq=1, Hkv=1, D=64, V=152064, ctx=(1, 1), gamma=4, logit_sd=sd,
+                   draft_div=1.0, draft_noise=0.8, **kw)
+    w = wl.make_sampler_inputs(spec, seed=11)
+    if clustered:
+        w.logits[..., :clustered] += 6.0
+    cfg = cfg_of(spec)
+    ref = oracle.sampler.accept_chain_batch(w.logits.numpy(), w.draft_probs.numpy(),
+                                            w.draft_tokens.numpy(), w.uniforms.numpy(), cfg,
+                                            want_p=True)
+    for want_p in (True, False):
+        gpu = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg, want_p)
+        compare(gpu, ref, max_flag_frac=1.0 if name == "flat_topp" else 0.5)
+        if want_p:
+            check_p(gpu["p"], ref, w.logits.numpy(), cfg)
 
 
 # ------------------------------------------------------------------ tree
