@@ -119,6 +119,8 @@ struct Sh {
   unsigned long long red_u[NW];
   unsigned long long zk, zcut;
   uint32_t oct[64];  // this CTA's per-octave counts [0, 32) and m16 sums [32, 64)
+  uint32_t octc[32];            // one-CTA rows: per-octave counts
+  unsigned long long octm[32];  // and m16 sums
   int list_n[NW];
   int bi[8];
   Cut cut;
@@ -153,14 +155,14 @@ SPEC_DEV uint64_t l2_keep_policy() {
 }
 SPEC_DEV float4 ldg_keep4(const float4* p, uint64_t pol) {
   float4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p), "l"(pol));
   return v;
 }
 SPEC_DEV float ldg_keep(const float* p, uint64_t pol) {
   float v;
-  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
   return v;
 }
 
@@ -228,7 +230,35 @@ SPEC_DEV unsigned long long fx44(uint32_t bits) {
   return sh >= 0 ? sig << sh : (sh > -24 ? sig >> (-sh) : 0ull);
 }
 
-constexpr double kFx = 17592186044416.0;  // 2^44
+// x * 2^44 truncated toward zero, from the float's fields (|x| < 2^19)
+SPEC_DEV long long fx44_signed(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const int f = (int)((b >> 23) & 0xFFu);
+  if (f == 0) return 0ll;
+  const unsigned long long sig = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = f - 106;
+  const unsigned long long v = sh >= 0 ? sig << min(sh, 39) : (sh > -24 ? sig >> (-sh) : 0ull);
+  return (b >> 31) ? -(long long)v : (long long)v;
+}
+
+// a float pair's sum in units of 2^-44 (a non-negative total)
+SPEC_DEV unsigned long long fx44_pair(float hi, float lo) {
+  return (unsigned long long)(fx44_signed(hi) + fx44_signed(lo));
+}
+
+// floor(z * f) for a float f in (0, 1): exact, on the 128-bit product
+SPEC_DEV unsigned long long mul_frac(unsigned long long z, float f) {
+  const uint32_t b = __float_as_uint(f);
+  const int ex = (int)((b >> 23) & 0xFFu);
+  if (ex == 0) return 0ull;
+  const unsigned long long sig = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = 150 - ex;  // f = sig * 2^-sh; sh >= 24 for f < 1
+  if (sh <= 0) return z;
+  const unsigned long long lo = z * sig, hi = __umul64hi(z, sig);
+  if (sh >= 128) return 0ull;
+  if (sh >= 64) return hi >> (sh - 64);
+  return (hi << (64 - sh)) | (lo >> sh);
+}
 
 SPEC_DEV float residual_w(float v, float invw, float qv) {
   return fmaxf(__fmaf_rn(v, invw, -qv), 0.f);
@@ -763,8 +793,9 @@ SPEC_DEV int next_child(const int* par, int v, int c, int R) {
 // kidx: the top-k cut's index among the members (-1: no top-k); members: the
 // count in the range (-1: not known from the histogram).
 template <int NT, class OctF, class BinF>
-SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, double zall, OctF octf,
-                         BinF binf, int* mode_o, int* b_lo_o, int* b_hi_o, int* kidx_o) {
+SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, unsigned long long zfx,
+                         OctF octf, BinF binf, int* mode_o, int* b_lo_o, int* b_hi_o,
+                         int* kidx_o) {
   const int lane = threadIdx.x & 31;
   unsigned long long oc_c = 0, oc_m = 0;
   octf(lane, oc_c, oc_m);
@@ -821,7 +852,7 @@ SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, double za
         const unsigned long long im = scan(bmass);
         const unsigned long long abk =
             __shfl_sync(kFull, pm, ok) + __shfl_sync(kFull, im - bmass, jk);
-        const unsigned long long thr = (unsigned long long)((double)top_p * (double)abk);
+        const unsigned long long thr = mul_frac(abk, top_p);
         const unsigned h2 = __ballot_sync(kFull, xm >= thr);
         int ol = h2 ? __ffs(h2) - 1 : ok;
         if (ol > ok) ol = ok;
@@ -852,8 +883,7 @@ SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, double za
       }
     }
   } else {
-    const double zd = zall;
-    const unsigned long long thr = (unsigned long long)((double)top_p * zd * kFx);
+    const unsigned long long thr = mul_frac(zfx, top_p);
     const unsigned h = __ballot_sync(kFull, xm >= thr);
     if (!h) {
       mode = 2;
@@ -1256,7 +1286,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       if (warp == 0) {
         int mode, bl, bh, kx;
         find_range<NT>(
-            topk, topp, p.top_k, p.top_p, (double)zah + (double)zal,
+            topk, topp, p.top_k, p.top_p, fx44_pair(zah, zal),
             [&](int o, unsigned long long& c, unsigned long long& mm) {
               for (int r = 0; r < CS; ++r) {
                 if (topk) c += dsmem_ld_u32(&sh.oct[o], r);
@@ -1343,7 +1373,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
             }
           }
           if (!select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
-                              (unsigned long long)(((double)zah + (double)zal) * kFx), gkey, gbits,
+                              fx44_pair(zah, zal), gkey, gbits,
                               &cut, &zkept, sh))
             tmode = 2;  // the rounded bin masses placed the cut one bin off
         }
@@ -1620,6 +1650,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   if (threadIdx.x == 0) {
     sh.token_in = -1;
     sh.eprobe = 0.f;
+    sh.bi[4] = 0;  // members found so far
   }
   if (trunc)
     for (int k = threadIdx.x; k < kHist; k += NT) {
@@ -1717,9 +1748,10 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // E bits at or above edge_f <=> bin <= bf
     const uint32_t edge_f = listing ? (uint32_t)(0x3F7FFFFF - ((bf + 1) << 18) + 1) : 0xFFFFFFFFu;
 
-    // ---- 3. Z (E recomputed, compensated per thread; four at a time); with a
-    // floor, one bit per id for the elements at or above it, else the
-    // histogram of every element
+    // ---- 3. Z (E recomputed, compensated per thread), each warp over its own
+    // range; with a floor, one bit per id for the elements at or above it (a
+    // word of 32 consecutive ids per eight lanes), else the histogram of every
+    // element
     const bool zhist = trunc && !listing;
     float zs = 0.f, zc = 0.f;
     auto kahan = [&](float x) {
@@ -1728,58 +1760,44 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       zc = (t - zs) - y;
       zs = t;
     };
-    for (int b0 = 0; b0 < n4; b0 += 4 * NT) {  // warp-uniform trip count
-      float4 v[4];
+    for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
+      float lv[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load4(s0 + 128 * u + 4 * lane, lv[u]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int k4 = b0 + u * NT + threadIdx.x;
-        v[u] = k4 < n4 ? ldg_keep4(l4 + k4, pol) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
+        const int k = s0 + 128 * u + 4 * lane;
+        float e[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k4 = b0 + u * NT + threadIdx.x;
-        const float e0 = Eof(v[u].x), e1 = Eof(v[u].y), e2 = Eof(v[u].z), e3 = Eof(v[u].w);
-        kahan((e0 + e1) + (e2 + e3));
-        if (zhist && k4 < n4) {
-          hist_e(e0);
-          hist_e(e1);
-          hist_e(e2);
-          hist_e(e3);
+        for (int j = 0; j < 4; ++j) e[j] = Eof(lv[u][j]);  // 0 past the range
+        kahan((e[0] + e[1]) + (e[2] + e[3]));
+        if (zhist) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (k + j < r1) hist_e(e[j]);
         }
         if (listing) {
-          // ids 4 k4 .. 4 k4 + 3; eight lanes make one word of 32 ids
-          uint32_t nib = (__float_as_uint(e0) >= edge_f ? 1u : 0u) |
-                         (__float_as_uint(e1) >= edge_f ? 2u : 0u) |
-                         (__float_as_uint(e2) >= edge_f ? 4u : 0u) |
-                         (__float_as_uint(e3) >= edge_f ? 8u : 0u);
-          if (k4 >= n4) nib = 0u;
+          uint32_t nib = (__float_as_uint(e[0]) >= edge_f ? 1u : 0u) |
+                         (__float_as_uint(e[1]) >= edge_f ? 2u : 0u) |
+                         (__float_as_uint(e[2]) >= edge_f ? 4u : 0u) |
+                         (__float_as_uint(e[3]) >= edge_f ? 8u : 0u);
           nib <<= 4 * (lane & 7);
           nib |= __shfl_xor_sync(kFull, nib, 1);
           nib |= __shfl_xor_sync(kFull, nib, 2);
           nib |= __shfl_xor_sync(kFull, nib, 4);
-          if ((lane & 7) == 0 && k4 < n4) fbits[k4 >> 3] = nib;
+          if ((lane & 7) == 0 && k < r1) fbits[k >> 5] = nib;
         }
-      }
-    }
-    // rows without 16-byte vectors: one id per thread, one word per warp
-    for (int k0 = 4 * n4; k0 < V; k0 += NT) {
-      const int k = k0 + threadIdx.x;
-      const float e = k < V ? Eof(ldg_keep(lrow + k, pol)) : 0.f;
-      kahan(e);
-      if (zhist && k < V) hist_e(e);
-      if (listing) {
-        const unsigned word = __ballot_sync(kFull, k < V && __float_as_uint(e) >= edge_f);
-        if (lane == 0 && k < V) fbits[k >> 5] = word;
       }
     }
     if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(__ldg(lrow + probe));
 
     // ---- 4. the candidate lists: each warp lists the flagged ids of its
-    // range in id order, then their logits; the histogram of the listed
-    // elements (they are exactly those of bins <= bf)
+    // range in id order, then loads their logits; the histogram of the listed
+    // elements (exactly those of bins <= bf); if a list overflowed, of every
+    // element
     int cntw = 0;
     if (listing) {
-      __syncthreads();  // flag words complete
+      __syncwarp();  // the warp's flag words are written
       const int w0 = (r0 + 31) >> 5, w1 = (r1 + 31) >> 5;  // r0: a multiple of 32, or V
       for (int wb = w0; wb < w1; wb += 32) {
         const int wd = wb + lane;
@@ -1800,72 +1818,79 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
         cntw += __shfl_sync(kFull, incl, 31);
       }
-      if (lane == 0) sh.list_n[warp] = cntw;
-    }
-    const bool fit = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
-    // lists hold every element that can be kept (ids, logits)
-    bool cand_lists = listing && fit;
-    if (cand_lists) {
-      const int cnt = cntw;
-      for (int j0 = 0; j0 < cnt; j0 += 32 * 8) {
-        float lvv[8];
+      if (cntw <= WCAP) {
+        __syncwarp();
+        float lvv[WCAP / 32];  // every logit of the list in flight at once
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = j0 + 32 * u + lane;
-          lvv[u] = j < cnt ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
+        for (int u = 0; u < WCAP / 32; ++u) {
+          const int j = 32 * u + lane;
+          lvv[u] = j < cntw ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = j0 + 32 * u + lane;
-          if (j < cnt) {
+        for (int u = 0; u < WCAP / 32; ++u) {
+          const int j = 32 * u + lane;
+          if (j < cntw) {
             lval[warp * WCAP + j] = lvv[u];
             hist_e(Eof(lvv[u]));
           }
         }
       }
-    } else if (listing) {
-      // a list overflowed: the histogram of every element
+    }
+    if (lane == 0) sh.list_n[warp] = cntw;
+    const bool fit = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
+    // lists hold every element that can be kept (ids, logits)
+    bool cand_lists = listing && fit;
+    if (listing && !fit) {
+      for (int k = threadIdx.x; k < kHist; k += NT) {
+        hcnt[k] = 0u;
+        hm[k] = 0u;
+      }
+      __syncthreads();
       sweep([&](int, float l) { hist_e(Eof(l)); });
       bf = -1;
     }
     const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
     const float zl = block_sum_f<NT>(-zc, sh);
     const float e_probe = sh.eprobe;
-    const double zall = (double)zh + (double)zl;
+    const unsigned long long zfx = fx44_pair(zh, zl);  // Z in units of 2^-44
 
     Cut cut{0, 0.f, 0u, INT_MAX};
     float zkept = zh + zl;
     if (trunc) {
       // ---- 5. the cut: bin range, members, selection (or the radix fallback)
+      // every warp runs the search on the octave totals (a lone warp whose
+      // siblings wait at a barrier runs its shuffles far slower)
+      int f_mode = 2, f_lo = 0, f_hi = 0, f_k = -1;
       auto run_find = [&]() {
-        if (warp == 0) {
-          int mode, bl, bh, kx;
-          find_range<NT>(
-              topk, topp, p.top_k, p.top_p, zall,
-              [&](int o, unsigned long long& c, unsigned long long& mm) {
-                for (int j = 0; j < 32; ++j) {
-                  const int bb = 32 * o + ((j + o) & 31);  // lanes start at different banks
-                  if (topk) c += hcnt[bb];
-                  if (topp) mm += hm[bb];
-                }
-              },
-              [&](int bb, unsigned long long& c, unsigned long long& mm) {
-                if (topk) c += hcnt[bb];
-                if (topp) mm += hm[bb];
-              },
-              &mode, &bl, &bh, &kx);
+        {  // warp o: the totals of octave o
+          uint32_t c = topk ? hcnt[32 * warp + lane] : 0u;
+          unsigned long long mm = topp ? hm[32 * warp + lane] : 0u;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            c += __shfl_xor_sync(kFull, c, o);
+            mm += __shfl_xor_sync(kFull, mm, o);
+          }
           if (lane == 0) {
-            sh.bi[0] = mode;
-            sh.bi[1] = bl;
-            sh.bi[2] = bh;
-            sh.bi[3] = kx;
-            sh.bi[4] = 0;
+            sh.octc[warp] = c;
+            sh.octm[warp] = mm;
           }
         }
         __syncthreads();
+        find_range<NT>(
+            topk, topp, p.top_k, p.top_p, zfx,
+            [&](int o, unsigned long long& c, unsigned long long& mm) {
+              c += sh.octc[o];
+              mm += sh.octm[o];
+            },
+            [hcnt, hm, topk, topp](int bb, unsigned long long& c, unsigned long long& mm) {
+              if (topk) c += hcnt[bb];
+              if (topp) mm += hm[bb];
+            },
+            &f_mode, &f_lo, &f_hi, &f_k);
+        __syncthreads();  // the totals may be rewritten by a second search
       };
       run_find();
-      int tmode = sh.bi[0];
+      int tmode = f_mode;
       if (tmode == 2 && cand_lists) {
         // the cut lies below the listed bins: histogram the rest, search again
         sweep([&](int, float l) {
@@ -1875,10 +1900,10 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         });
         __syncthreads();
         run_find();
-        tmode = sh.bi[0];
+        tmode = f_mode;
         cand_lists = false;
       }
-      const int b_lo = sh.bi[1], b_hi = sh.bi[2], kidx = sh.bi[3];
+      const int b_lo = f_lo, b_hi = f_hi, kidx = f_k;
       if (tmode == 1) {
         // members of bins [b_lo, b_hi] and the exact mass above them; a logit
         // pre-filter (with margin) skips the E of elements below the range
@@ -1954,7 +1979,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           const unsigned long long key = t < total ? xkey[t] : 0ull;
           const uint32_t eb = t < total ? xbits[t] : 0u;
           if (!select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
-                              (unsigned long long)(zall * kFx), xkey, xbits, &cut, &zkept, sh))
+                              zfx, xkey, xbits, &cut, &zkept, sh))
             tmode = 2;
         }
       }
