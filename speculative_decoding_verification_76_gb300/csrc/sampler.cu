@@ -388,11 +388,14 @@ struct Items {
   bool listed;
   const uint16_t* lists;  // NW x (kListPerCTA / NW)
   int r0, r1;             // this warp's range [r0, r1)
-  SPEC_DEV int count(const Sh<NW>& sh) const {
-    return listed ? sh.list_n[threadIdx.x >> 5] : r1 - r0;
+  int rw, n;              // every warp's range: [min(w rw, n), min((w + 1) rw, n))
+  SPEC_DEV int count(const Sh<NW>& sh) const { return count_of(threadIdx.x >> 5, sh); }
+  SPEC_DEV int at(int j) const { return at_of(threadIdx.x >> 5, j); }
+  SPEC_DEV int count_of(int w, const Sh<NW>& sh) const {
+    return listed ? sh.list_n[w] : min((w + 1) * rw, n) - min(w * rw, n);
   }
-  SPEC_DEV int at(int j) const {
-    return listed ? (int)lists[(threadIdx.x >> 5) * (kListPerCTA / NW) + j] : r0 + j;
+  SPEC_DEV int at_of(int w, int j) const {
+    return listed ? (int)lists[w * (kListPerCTA / NW) + j] : min(w * rw, n) + j;
   }
 };
 
@@ -559,49 +562,46 @@ SPEC_DEV int locate(const float* buf, const Items<NT / 32>& it, int lo, float u,
     base_ow = base_lw;
   }
   if (ow < 0) return -1;  // unreachable: the owner CTA has positive weight
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == ow) {
-    const int cnt = it.count(sh);
-    const int c = ((cnt + 31) / 32) | 1;  // odd chunk length: conflict-free shared reads
-    const int j0 = min(lane * c, cnt), j1 = min(j0 + c, cnt);
-    float ls = 0.f;
-    for (int j = j0; j < j1; ++j) ls += buf[it.at(j)];
-    const float tw = target - base_ow;  // the crossing, relative to the warp's start
-    float incl = ls;
+  // every warp walks the owning warp's items (a lone warp whose siblings wait
+  // at a barrier runs its shuffles far slower)
+  const int lane = threadIdx.x & 31;
+  const int cnt = it.count_of(ow, sh);
+  const int c = ((cnt + 31) / 32) | 1;  // odd chunk length: conflict-free shared reads
+  const int j0 = min(lane * c, cnt), j1 = min(j0 + c, cnt);
+  float ls = 0.f;
+  for (int j = j0; j < j1; ++j) ls += buf[it.at_of(ow, j)];
+  const float tw = target - base_ow;  // the crossing, relative to the warp's start
+  float incl = ls;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(kFull, ls > 0.f && incl > tw);
-    const unsigned nz = __ballot_sync(kFull, ls > 0.f);
-    const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
-    int found = -1;
-    if (lane == L) {
-      const float tl = tw - (incl - ls);  // relative to this lane's chunk
-      float run = 0.f;
-      int lastk = -1;
-      for (int j = j0; j < j1; ++j) {
-        const int k = it.at(j);
-        const float v = buf[k];
-        if (v > 0.f) {
-          lastk = k;
-          run += v;
-          if (run > tl) {
-            found = k;
-            break;
-          }
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned hit = __ballot_sync(kFull, ls > 0.f && incl > tw);
+  const unsigned nz = __ballot_sync(kFull, ls > 0.f);
+  const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
+  int found = -1;
+  if (lane == L) {
+    const float tl = tw - (incl - ls);  // relative to this lane's chunk
+    float run = 0.f;
+    int lastk = -1;
+    for (int j = j0; j < j1; ++j) {
+      const int k = it.at_of(ow, j);
+      const float v = buf[k];
+      if (v > 0.f) {
+        lastk = k;
+        run += v;
+        if (run > tl) {
+          found = k;
+          break;
         }
       }
-      if (found < 0) found = lastk;  // rounding left the crossing just past the end
     }
-    found = __shfl_sync(kFull, found, L < 0 ? 0 : L);
-    if (lane == 0) sh.bi[7] = (L < 0 || found < 0) ? INT_MAX : lo + found;
+    if (found < 0) found = lastk;  // rounding left the crossing just past the end
   }
-  __syncthreads();
-  const int t = sh.bi[7];
-  __syncthreads();
-  return t == INT_MAX ? -1 : t;
+  found = __shfl_sync(kFull, found, L < 0 ? 0 : L);
+  __syncthreads();  // callers may rewrite buf
+  return (L < 0 || found < 0) ? -1 : lo + found;
 }
 
 // ---------------------------------------------------------------- exact radix fallback
@@ -1059,7 +1059,7 @@ SPEC_DEV void finish_row(const SP& p, int row, const Outcome& oc, Sh<NW>& sh) {
 //   tree node v: the first accepted child (residual p' updated after each
 //     rejected child) or, if none, the final token drawn from p'.
 // The cluster that finishes a sequence's last row assembles the sequence.
-template <int NT, bool FAST>
+template <int NT, bool FAST, bool TR>
 __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   constexpr int NW = NT / 32;
   constexpr int kWL = kListPerCTA / NW;
@@ -1089,9 +1089,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   const int n = max(0, min(p.slice, p.V - lo));
   const float* lrow_full = p.logits + (size_t)row * p.V;
   const float* lrow = lrow_full + lo;
-  const bool topk = p.top_k > 0 && p.top_k < p.V;
-  const bool topp = p.top_p > 0.f && p.top_p < 1.f;
-  const bool trunc = !p.greedy && (topk || topp);
+  // TR = false: rows without top-k / top-p (the truncation code is compiled out)
+  const bool topk = TR && p.top_k > 0 && p.top_k < p.V;
+  const bool topp = TR && p.top_p > 0.f && p.top_p < 1.f;
+  const bool trunc = TR && !p.greedy && (topk || topp);
   int ph = 0;
 
   // ---- 0. setup: barrier, histogram, tree shape, this row's probe token
@@ -1404,7 +1405,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
     // ---- 6. (tree, p_out: on first use) zero the cut-off tail in place and
     // list each warp's kept positions
     const int rw = ((n + NW - 1) / NW + 3) / 4 * 4;
-    Items<NW> it{false, lists, min(warp * rw, n), min((warp + 1) * rw, n)};
+    Items<NW> it{false, lists, min(warp * rw, n), min((warp + 1) * rw, n), rw, n};
     bool kept_ready = !trunc, zeroed = !trunc;
     // zero: also clear buf outside the kept set (needed where buf is read by
     // position: the tree's probe values and p_out)
@@ -1592,7 +1593,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 constexpr int kSNT = 1024;
 constexpr int kSCap = 16384;    // list entries per row (kSCap / 32 per warp)
 constexpr int kSBudget = 10240; // candidates a row's floor aims at (sampled estimate)
-constexpr int kSWords = 8192;   // flag words: rows of up to 32 * kSWords ids are listed
+constexpr int kSListMaxV = 163840;  // rows up to this long are listed (one flag bit per id)
 
 template <bool FAST>
 __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
@@ -1604,7 +1605,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   uint32_t* xbits = reinterpret_cast<uint32_t*>(xkey + NT);                          // NT
   int* lid = reinterpret_cast<int*>(xbits + NT);                                      // kSCap
   float* lval = reinterpret_cast<float*>(lid + kSCap);                                // kSCap
-  uint32_t* fbits = reinterpret_cast<uint32_t*>(lval + kSCap);                        // kSWords
+  uint32_t* fbits = reinterpret_cast<uint32_t*>(lval + kSCap);  // (V + 31) / 32 when listing
   const RadixScratch rs{reinterpret_cast<uint32_t*>(xkey), xkey + 256, xkey + 768,
                         reinterpret_cast<uint32_t*>(xkey) + 2048};
   __shared__ Sh<NW> sh;
@@ -1730,7 +1731,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // sampled count at or above it stays within the list budget; the elements
     // of bins <= bf are listed.  -1: no floor (every element histogrammed)
     int bf = -1;
-    if (trunc && V <= 32 * kSWords) {
+    if (trunc && V <= kSListMaxV) {
       const float budget =
           topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
       const int ns = (int)(budget * (float)NT / (float)V);
@@ -1820,18 +1821,20 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       }
       if (cntw <= WCAP) {
         __syncwarp();
-        float lvv[WCAP / 32];  // every logit of the list in flight at once
+        for (int j0 = 0; j0 < cntw; j0 += 512) {
+          float lvv[16];  // sixteen logits of the list in flight per lane
 #pragma unroll
-        for (int u = 0; u < WCAP / 32; ++u) {
-          const int j = 32 * u + lane;
-          lvv[u] = j < cntw ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
-        }
+          for (int u = 0; u < 16; ++u) {
+            const int j = j0 + 32 * u + lane;
+            lvv[u] = j < cntw ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
+          }
 #pragma unroll
-        for (int u = 0; u < WCAP / 32; ++u) {
-          const int j = 32 * u + lane;
-          if (j < cntw) {
-            lval[warp * WCAP + j] = lvv[u];
-            hist_e(Eof(lvv[u]));
+          for (int u = 0; u < 16; ++u) {
+            const int j = j0 + 32 * u + lane;
+            if (j < cntw) {
+              lval[warp * WCAP + j] = lvv[u];
+              hist_e(Eof(lvv[u]));
+            }
           }
         }
       }
@@ -2349,11 +2352,11 @@ size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
   return off;
 }
 
-template <int NT, bool FAST>
+template <int NT, bool FAST, bool TR>
 spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t st) {
   static bool attr_set = false;  // once, at the largest size, so graph captures need no setup
   if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_kernel<NT, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sampler_kernel<NT, FAST, TR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_smem(kMaxSliceBytes, true)) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
@@ -2370,12 +2373,13 @@ spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sampler_kernel<NT, FAST>, prm) != cudaSuccess) return SPEC_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sampler_kernel<NT, FAST, TR>, prm) != cudaSuccess) return SPEC_ECUDA;
   return launch_status();
 }
 
-size_t stream_smem() {
-  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8 + (size_t)kSWords * 4;
+size_t stream_smem(int V) {
+  const size_t words = V <= kSListMaxV ? (size_t)(V + 31) / 32 : 0;
+  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8 + words * 4;
 }
 
 template <bool FAST>
@@ -2383,14 +2387,14 @@ spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(sampler_stream_kernel<FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem()) != cudaSuccess)
+                             (int)stream_smem(kSListMaxV)) != cudaSuccess)
       return SPEC_ECUDA;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows, 1, 1);
   cfg.blockDim = dim3(kSNT, 1, 1);
-  cfg.dynamicSmemBytes = stream_smem();
+  cfg.dynamicSmemBytes = stream_smem(prm.V);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (its radix fallback
@@ -2421,11 +2425,19 @@ spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
   const SampPlan pl = plan_sampler(B, R, V, prm.qsm != 0);
   if ((size_t)pl.slice * 4 > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
   prm.slice = pl.slice;
-  if (prm.p_out)
-    return pl.NT == 512 ? launch_nt<512, false>(prm, pl, B * R, st)
-                        : launch_nt<256, false>(prm, pl, B * R, st);
-  return pl.NT == 512 ? launch_nt<512, true>(prm, pl, B * R, st)
-                      : launch_nt<256, true>(prm, pl, B * R, st);
+  const bool tr = trunc && !prm.greedy;
+  if (prm.p_out) {
+    if (tr)
+      return pl.NT == 512 ? launch_nt<512, false, true>(prm, pl, B * R, st)
+                          : launch_nt<256, false, true>(prm, pl, B * R, st);
+    return pl.NT == 512 ? launch_nt<512, false, false>(prm, pl, B * R, st)
+                        : launch_nt<256, false, false>(prm, pl, B * R, st);
+  }
+  if (tr)
+    return pl.NT == 512 ? launch_nt<512, true, true>(prm, pl, B * R, st)
+                        : launch_nt<256, true, true>(prm, pl, B * R, st);
+  return pl.NT == 512 ? launch_nt<512, true, false>(prm, pl, B * R, st)
+                      : launch_nt<256, true, false>(prm, pl, B * R, st);
 }
 
 spec_status check_cfg(const spec_sampler* cfg) {
