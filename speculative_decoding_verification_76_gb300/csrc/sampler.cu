@@ -1129,6 +1129,12 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   }
   // full-vocabulary residuals read q from shared memory (loaded with the logits)
   const bool q_sh = p.qsm && qrow != nullptr && n > 0;
+  // the chain test's operands, loaded now: their latency hides under the slice load
+  const bool chain_test = !p.tree && i < R - 1;
+  const float u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
+  const float u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+  const float q_probe =
+      (chain_test && qrow != nullptr && probe >= 0 && probe < p.V) ? __ldg(&qrow[probe]) : 0.f;
 
   // ---- 1. the slice (and q's) into shared memory
   if (n > 0) {
@@ -1466,7 +1472,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       for (int k = threadIdx.x; k < n; k += NT) dst[k] = buf[k] * invz;
     }
 
-    const float u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    const float u_final = u_last;
     const float* qlo = q_sh ? qb : (qrow ? qrow + lo : nullptr);
     if (!p.tree) {
       // ---- 7a. chain: the row's test, then its correction or bonus draw
@@ -1474,11 +1480,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       if (i < R - 1) {
         const int x = probe;
         const bool xin = x >= 0 && x < p.V;
-        const float qx = xin ? __ldg(&qrow[x]) : 0.f;
+        const float qx = xin ? q_probe : 0.f;
         const float px = (xin && e_probe > 0.f && cut_keeps(cut, e_probe, x, lrow_full))
                              ? e_probe * invz : 0.f;
         if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
-        oc.accept = (__ldg(&p.u[(size_t)b * R + i]) * qx < px) ? 1 : 0;
+        oc.accept = (u_test * qx < px) ? 1 : 0;
         resid = !oc.accept;
       }
       drew = i == R - 1 || resid;
@@ -1679,6 +1685,13 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     else if (i < R - 1)
       qrow = p.q + ((size_t)b * (R - 1) + i) * V;
   }
+  // the chain test's operands, loaded now: their latency hides under the sweeps
+  const bool chain_test = !p.tree && i < R - 1;
+  const float u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
+  const float u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+  const float q_probe =
+      (chain_test && qrow != nullptr && probe >= 0 && probe < V) ? __ldg(&qrow[probe]) : 0.f;
+  const float l_probe = (probe >= 0 && probe < V) ? __ldg(lrow + probe) : 0.f;
 
   // each warp owns one contiguous id range of the row (a multiple of 32 long);
   // four logits of ids k..k+3 at a time (-inf past the range)
@@ -1790,7 +1803,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
       }
     }
-    if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(__ldg(lrow + probe));
+    if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(l_probe);
 
     // ---- 4. the candidate lists: each warp lists the flagged ids of its
     // range in id order, then loads their logits; the histogram of the listed
@@ -2229,17 +2242,17 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       return t;
     };
 
-    const float u_final = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    const float u_final = u_last;
     if (!p.tree) {
       // ---- 7a. chain: the row's test, then its correction or bonus draw
       bool resid = false;
       if (i < R - 1) {
         const int x = probe;
         const bool xin = x >= 0 && x < V;
-        const float qx = xin ? __ldg(&qrow[x]) : 0.f;
-        const float px = (xin && e_probe > 0.f && kept_l(__ldg(lrow + x), x)) ? e_probe * invz : 0.f;
+        const float qx = xin ? q_probe : 0.f;
+        const float px = (xin && e_probe > 0.f && kept_l(l_probe, x)) ? e_probe * invz : 0.f;
         if (qx == 0.f) oc.status |= SPEC_SEQ_QZERO;
-        oc.accept = (__ldg(&p.u[(size_t)b * R + i]) * qx < px) ? 1 : 0;
+        oc.accept = (u_test * qx < px) ? 1 : 0;
         resid = !oc.accept;
       }
       if (i == R - 1 || resid) {
