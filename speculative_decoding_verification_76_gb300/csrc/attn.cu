@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const AttnParams p) {
 // out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M), one warp per output row.
 // Launched as a programmatic dependent of the partial pass: everything up to
 // griddepcontrol.wait overlaps the partial pass's tail.
-template <typename OutT>
+template <typename OutT, int kBatch>
 __global__ void __launch_bounds__(128) attn_combine(const AttnParams p, OutT* __restrict__ out,
                                                    float* __restrict__ lse_out) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -498,12 +498,11 @@ __global__ void __launch_bounds__(128) attn_combine(const AttnParams p, OutT* __
   if (!live) return;
   const int D = p.D;
   const int per = D / 32;  // 4 (D = 128) or 2 (D = 64) floats per lane
+  // one pass, kBatch partials in flight at a time; the running maximum M
+  // rescales the sums when a later batch raises it (one batch: no rescale)
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(&p.lse_part[prow0 + s]));
-  M = warp_max(M);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float L = 0.f;
-  constexpr int kBatch = 8;
   for (int s0 = 0; s0 < ns; s0 += kBatch) {
     float ls[kBatch];
     float4 v[kBatch];
@@ -511,9 +510,20 @@ __global__ void __launch_bounds__(128) attn_combine(const AttnParams p, OutT* __
     for (int j = 0; j < kBatch; ++j) {  // independent loads, all in flight together
       const int s = s0 + j;
       ls[j] = s < ns ? __ldcg(&p.lse_part[prow0 + s]) : -INFINITY;
-      const float* src = p.o_part + (prow0 + min(s, ns - 1)) * D + per * lane;
-      v[j] = per == 4 ? __ldcg(reinterpret_cast<const float4*>(src))
-                      : make_float4(__ldcg(src), __ldcg(src + 1), 0.f, 0.f);
+      const float* src = p.o_part + (prow0 + s) * D + per * lane;
+      v[j] = s >= ns     ? make_float4(0.f, 0.f, 0.f, 0.f)
+             : per == 4 ? __ldcg(reinterpret_cast<const float4*>(src))
+                        : make_float4(__ldcg(src), __ldcg(src + 1), 0.f, 0.f);
+    }
+    float bm = ls[0];
+#pragma unroll
+    for (int j = 1; j < kBatch; ++j) bm = fmaxf(bm, ls[j]);
+    if (bm > M) {
+      const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - bm);
+      L *= sc;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] *= sc;
+      M = bm;
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
@@ -552,8 +562,11 @@ spec_status launch_combine(const AttnParams& prm, OutT* out, float* lse_out, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_combine<OutT>, prm, out, lse_out) != cudaSuccess)
-    return SPEC_ECUDA;
+  // few splits: eight partials a pass (fewer registers, more warps resident)
+  const cudaError_t e =
+      prm.S <= 8 ? cudaLaunchKernelEx(&cfg, attn_combine<OutT, 8>, prm, out, lse_out)
+                 : cudaLaunchKernelEx(&cfg, attn_combine<OutT, 16>, prm, out, lse_out);
+  if (e != cudaSuccess) return SPEC_ECUDA;
   return launch_status();
 }
 

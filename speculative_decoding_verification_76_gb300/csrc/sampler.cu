@@ -1129,21 +1129,28 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   }
   // full-vocabulary residuals read q from shared memory (loaded with the logits)
   const bool q_sh = p.qsm && qrow != nullptr && n > 0;
-  // the chain test's operands, loaded now: their latency hides under the slice load
   const bool chain_test = !p.tree && i < R - 1;
-  const float u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
-  const float u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
-  const float q_probe =
-      (chain_test && qrow != nullptr && probe >= 0 && probe < p.V) ? __ldg(&qrow[probe]) : 0.f;
+  float u_test = 0.f, u_last = 0.f, q_probe = 0.f;
+  // the chain test's operands, loaded after the slice copies are issued: their
+  // latency hides under the copies
+  auto load_test_operands = [&]() {
+    u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
+    u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+    q_probe = (chain_test && qrow != nullptr && probe >= 0 && probe < p.V) ? __ldg(&qrow[probe])
+                                                                           : 0.f;
+  };
 
   // ---- 1. the slice (and q's) into shared memory
+  if (n > 0 && p.bulk) {
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(&sh.bar, (uint32_t)n * (q_sh ? 8u : 4u));
+      bulk_load(buf, lrow, (uint32_t)n * 4u, &sh.bar);
+      if (q_sh) bulk_load(qb, qrow + lo, (uint32_t)n * 4u, &sh.bar);
+    }
+  }
+  load_test_operands();
   if (n > 0) {
     if (p.bulk) {
-      if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&sh.bar, (uint32_t)n * (q_sh ? 8u : 4u));
-        bulk_load(buf, lrow, (uint32_t)n * 4u, &sh.bar);
-        if (q_sh) bulk_load(qb, qrow + lo, (uint32_t)n * 4u, &sh.bar);
-      }
       mbar_wait(&sh.bar, 0, p.err);
     } else {
       for (int k = threadIdx.x; k < n; k += NT) buf[k] = __ldg(lrow + k);
@@ -1685,13 +1692,6 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     else if (i < R - 1)
       qrow = p.q + ((size_t)b * (R - 1) + i) * V;
   }
-  // the chain test's operands, loaded now: their latency hides under the sweeps
-  const bool chain_test = !p.tree && i < R - 1;
-  const float u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
-  const float u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
-  const float q_probe =
-      (chain_test && qrow != nullptr && probe >= 0 && probe < V) ? __ldg(&qrow[probe]) : 0.f;
-  const float l_probe = (probe >= 0 && probe < V) ? __ldg(lrow + probe) : 0.f;
 
   // each warp owns one contiguous id range of the row (a multiple of 32 long);
   // four logits of ids k..k+3 at a time (-inf past the range)
@@ -1725,6 +1725,13 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   __syncthreads();
   const bool bad = isnan(m) || m == INFINITY || m == -INFINITY;
   Outcome oc{0, -1, 0, bad ? 1 : 0};
+  // the chain test's operands, loaded now: their latency hides under the next sweep
+  const bool chain_test = !p.tree && i < R - 1;
+  const float u_test = chain_test ? __ldg(&p.u[(size_t)b * R + i]) : 0.f;
+  const float u_last = __ldg(&p.u[(size_t)b * R + (R - 1)]);
+  const float q_probe =
+      (chain_test && qrow != nullptr && probe >= 0 && probe < V) ? __ldg(&qrow[probe]) : 0.f;
+  const float l_probe = (probe >= 0 && probe < V) ? __ldg(lrow + probe) : 0.f;
 
   if (!bad) {
     const float nm = -m, lfloor = m - 150.f * p.T;
