@@ -1089,10 +1089,13 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   const int n = max(0, min(p.slice, p.V - lo));
   const float* lrow_full = p.logits + (size_t)row * p.V;
   const float* lrow = lrow_full + lo;
-  // TR = false: rows without top-k / top-p (the truncation code is compiled out)
+  // TR = false: untruncated, sampled chain rows (the truncation, tree and greedy
+  // code is compiled out: each CTA runs its program once and fetches it cold)
+  const bool tree = TR && p.tree != 0;
+  const bool greedy = TR && p.greedy != 0;
   const bool topk = TR && p.top_k > 0 && p.top_k < p.V;
   const bool topp = TR && p.top_p > 0.f && p.top_p < 1.f;
-  const bool trunc = TR && !p.greedy && (topk || topp);
+  const bool trunc = TR && !greedy && (topk || topp);
   int ph = 0;
 
   // ---- 0. setup: barrier, histogram, tree shape, this row's probe token
@@ -1106,7 +1109,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       hcnt[k] = 0u;
       hm[k] = 0u;
     }
-  if (p.tree)
+  if (tree)
     for (int c = threadIdx.x; c < R; c += NT) {
       sh.par[c] = p.parent[(size_t)b * R + c];
       sh.tok[c] = p.tokens[(size_t)b * R + c];
@@ -1114,22 +1117,22 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
   __syncthreads();
   // the token whose E this row's first test needs (-1: no test)
   int probe = -1;
-  if (!p.tree) {
+  if (!tree) {
     if (i < R - 1) probe = __ldg(&p.tokens[(size_t)b * (R - 1) + i]);
   } else {
     const int fc = next_child(sh.par, i, i, R);
     if (fc >= 0) probe = sh.tok[fc];
   }
   const float* qrow = nullptr;
-  if (!p.greedy && p.q) {
-    if (p.tree)
+  if (!greedy && p.q) {
+    if (tree)
       qrow = p.q + ((size_t)b * R + i) * p.V;
     else if (i < R - 1)
       qrow = p.q + ((size_t)b * (R - 1) + i) * p.V;
   }
   // full-vocabulary residuals read q from shared memory (loaded with the logits)
   const bool q_sh = p.qsm && qrow != nullptr && n > 0;
-  const bool chain_test = !p.tree && i < R - 1;
+  const bool chain_test = !tree && i < R - 1;
   float u_test = 0.f, u_last = 0.f, q_probe = 0.f;
   // the chain test's operands, loaded after the slice copies are issued: their
   // latency hides under the copies
@@ -1167,7 +1170,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
     for (int k4 = threadIdx.x; k4 < n4; k4 += NT) {
       const float4 v = b4[k4];
       mx = fmax_nan(fmax_nan(mx, v.x), fmax_nan(fmax_nan(v.y, v.z), v.w));
-      if (p.greedy) {
+      if (greedy) {
         if (v.x > best) { best = v.x; bid = 4 * k4; }
         if (v.y > best) { best = v.y; bid = 4 * k4 + 1; }
         if (v.z > best) { best = v.z; bid = 4 * k4 + 2; }
@@ -1177,7 +1180,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
     for (int k = 4 * n4 + threadIdx.x; k < n; k += NT) {
       const float v = buf[k];
       mx = fmax_nan(mx, v);
-      if (p.greedy && v > best) { best = v; bid = k; }
+      if (greedy && v > best) { best = v; bid = k; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1216,8 +1219,8 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 
   if (bad) {
     // no distribution: the sequence reports NONFINITE
-  } else if (p.greedy) {
-    if (!p.tree) {
+  } else if (greedy) {
+    if (!tree) {
       if (i < R - 1) oc.accept = (probe == argmax) ? 1 : 0;
     } else {
       oc.accept = -1;
@@ -1473,7 +1476,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       it.listed = __syncthreads_and(cntw <= kWL ? 1 : 0) != 0;
     };
     const float invz = 1.0f / zkept;
-    if (p.p_out) {
+    if (!FAST && p.p_out) {
       ensure_kept(true);
       float* dst = p.p_out + (size_t)row * p.V + lo;
       for (int k = threadIdx.x; k < n; k += NT) dst[k] = buf[k] * invz;
@@ -1481,7 +1484,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 
     const float u_final = u_last;
     const float* qlo = q_sh ? qb : (qrow ? qrow + lo : nullptr);
-    if (!p.tree) {
+    if (!tree) {
       // ---- 7a. chain: the row's test, then its correction or bonus draw
       bool resid = false;
       if (i < R - 1) {
@@ -2445,7 +2448,7 @@ spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
   const SampPlan pl = plan_sampler(B, R, V, prm.qsm != 0);
   if ((size_t)pl.slice * 4 > kMaxSliceBytes) return SPEC_EUNSUPPORTED;
   prm.slice = pl.slice;
-  const bool tr = trunc && !prm.greedy;
+  const bool tr = (trunc && !prm.greedy) || prm.tree || prm.greedy;  // else: the compact variant
   if (prm.p_out) {
     if (tr)
       return pl.NT == 512 ? launch_nt<512, false, true>(prm, pl, B * R, st)
