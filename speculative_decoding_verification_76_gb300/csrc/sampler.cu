@@ -1601,11 +1601,15 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 
 // ---------------------------------------------------------------- streaming kernel (many rows)
 // One 1024-thread CTA per target row, used for truncated sampling when many
-// rows run at once.  The row is read from global memory: once from HBM for
-// the maximum, then (E recomputed, the row now in L2) for Z and the
-// histogram, and for the members of the crossing bins.  The kept set (ids and
-// E) is then listed per warp in shared memory for the draws and the tree's
-// residuals.  No cluster exchanges: every SM works on its own rows.
+// rows run at once.  The row is read from global memory twice: from HBM for
+// the maximum (with one evenly spaced sample per thread), then, E recomputed
+// and the row now in L2, for Z, setting one bit per id at or above a floor
+// that the samples place so that about kSBudget ids pass.  Each warp turns
+// its bits into an id-ordered candidate list (ids and logits, shared memory);
+// the histogram, the members of the crossing bins, the kept set and the draws
+// all work on those lists.  A floor above the cut, or a list that overflows,
+// falls back to further sweeps of the row.  No cluster exchanges: every SM
+// works on its own rows.
 constexpr int kSNT = 1024;
 constexpr int kSCap = 16384;    // list entries per row (kSCap / 32 per warp)
 constexpr int kSBudget = 10240; // candidates a row's floor aims at (sampled estimate)
