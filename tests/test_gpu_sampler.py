@@ -263,18 +263,23 @@ STREAM_SHAPES = [
     # the sampled floor lies above the top-p cut (nearly flat row): the
     # histogram is completed and the cut found again; every token is lighter
     # than the flag margin, so p and the kept set carry the comparison
-    ("flat_topp", dict(temperature=1.0, top_p=0.9), 0.3, None),
+    ("flat_topp", dict(temperature=1.0, top_p=0.9), 0.3, None, 152064),
     # large top-k: the floor aims at the list budget
-    ("topk_3000", dict(temperature=1.0, top_k=3000), 3.0, None),
+    ("topk_3000", dict(temperature=1.0, top_k=3000), 3.0, None, 152064),
     # 3000 high logits at the start of the row: one warp's list overflows
-    ("clustered_topp", dict(temperature=1.0, top_p=0.9), 3.0, 3000),
+    ("clustered_topp", dict(temperature=1.0, top_p=0.9), 3.0, 3000, 152064),
+    # top-k beyond half the list budget: no floor, every element histogrammed
+    ("topk_6000", dict(temperature=1.0, top_k=6000), 3.0, None, 152064),
+    # rows longer than the flag words cover (and not a multiple of 4): no floor
+    ("long_row_topp", dict(temperature=1.0, top_p=0.9), 3.0, None, 170001),
 ]
 
 
-@pytest.mark.parametrize("name,kw,sd,clustered", STREAM_SHAPES, ids=[s[0] for s in STREAM_SHAPES])
-def test_many_rows_floor_fallbacks(name, kw, sd, clustered):
-    # 8 x 5 rows of a 152064-token vocabulary: the one-CTA-per-row path
-    spec = wl.Spec(name, B=8, Hq=1, Hkv=1, D=64, V=152064, ctx=(1, 1), gamma=4, logit_sd=sd,
+@pytest.mark.parametrize("name,kw,sd,clustered,V", STREAM_SHAPES,
+                         ids=[s[0] for s in STREAM_SHAPES])
+def test_many_rows_floor_fallbacks(name, kw, sd, clustered, V):
+    # 8 x 5 rows of a large vocabulary: the one-CTA-per-row path
+    spec = wl.Spec(name, B=8, Hq=1, Hkv=1, D=64, V=V, ctx=(1, 1), gamma=4, logit_sd=sd,
                    draft_div=1.0, draft_noise=0.8, **kw)
     w = wl.make_sampler_inputs(spec, seed=11)
     if clustered:
