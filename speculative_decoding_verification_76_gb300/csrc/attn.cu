@@ -616,9 +616,10 @@ bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_page
     if (units >= sms) {
       chunk = 2048;
     } else {
+      // about one wave of CTAs; long contexts take the longest chunk the page
+      // table slice holds (fewer, longer splits measured faster than 2048-token ones)
       const int S = std::max(1, sms / units);
       chunk = round_up((int)((max_kv + S - 1) / S), g);
-      if (chunk > 2048) chunk = 2048;
     }
   }
   chunk = std::max(g, std::min(chunk, kMaxChunk));
