@@ -112,6 +112,15 @@ def test_workspace_sizes(lib):
     assert sv.sample_workspace_size(4, 64, 128256) >= 256 + 4 * 64 * 16
 
 
+def test_split_plan_for_the_bench_shapes(lib):
+    # few units: about one wave of CTAs (8B-shaped: 8 KV heads x 17 splits of 512 tokens);
+    # units that fill the SMs: 4096-token chunks; explicit counts are honoured
+    assert sv.attn_num_splits(1, 8, 32, 8, 128, 16, 513) == 17
+    assert sv.attn_num_splits(64, 5, 32, 8, 128, 16, 1025) == 5  # 16400 tokens / 4096
+    assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193) == 33  # 131088 tokens / 4096
+    assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193, 128) >= 128
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(api, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
