@@ -2113,6 +2113,9 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // weights of the listed items (mode 1: max(0, v * invw - q) stored back):
     // per-warp sums in sh.wsum, the CTA total returned (fixed order)
     auto list_weights = [&](int mode, float invw) -> float {
+      // every warp is done with the previous weights (sh.wsum, and the list values
+      // a tree node's child test read from any warp's list) before they change
+      __syncthreads();
       const int cnt = min(sh.list_n[warp], WCAP);
       float acc = 0.f;
       for (int j = lane; j < cnt; j += 32) {
