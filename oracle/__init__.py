@@ -23,8 +23,13 @@ by eye, with no blocking, fusion or reordering beyond the definitions:
                 probability", "Greedy, sampling and the real sampler",
                 "Implementation roadmap and tests"; "Drafters and Speculative
                 Decoding", "Sampling needs a correction rule").
+  commit.py     the next step's KV bookkeeping: the processed length after
+                acceptance, the released pages, and a tree's accepted path
+                compacted into the next logical prefix ("Speculative
+                Decoding" (atlas), "Committed tokens versus cached states",
+                "Chains, trees and visibility").
 
 Every function is pinned by a test in tests/test_oracle_*.py against worked
 examples printed on the pages, closed forms or brute force.
 """
-from . import attention, sampler, tree  # noqa: F401
+from . import attention, commit, sampler, tree  # noqa: F401
