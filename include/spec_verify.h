@@ -274,6 +274,40 @@ spec_status spec_accept_sample_tree(const float* target_logits, const float* dra
 /* Copy the workspace error word to *host_err (synchronises `stream`). */
 spec_status spec_workspace_error(const void* workspace, int32_t* host_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * spec_kv_commit -- keep the verified states after acceptance.
+ * "Speculative Decoding" (atlas), "Committed tokens versus cached states":
+ * the states of accepted proposals are kept and the rejected suffix removed;
+ * the correction / bonus token's KV comes with the next pass.  "Chains,
+ * trees and visibility": a tree's accepted path is compacted into the next
+ * logical prefix so branch states are no longer addressable.
+ *
+ *   k_cache, v_cache [num_pages, page_size, Hkv, D], elem_bytes 2 (bf16) or
+ *            4 (fp32), 16-byte aligned, updated in place (trees only).
+ *   block_table [B, max_pages] int32; ctx_len [B] int32: block row j was
+ *            written at cache position ctx_len[b] + j.
+ *   accepted_len [B] int32: drafts accepted (0 .. R-1).
+ *   path     [B, R] int32 (NULL: a chain, nothing moves): node 0 then the
+ *            accepted nodes in order (entries past accepted_len[b] ignored);
+ *            node ids strictly increase.  The K/V rows of path[b][k] move to
+ *            position ctx_len[b] + k (every row is read before any is written).
+ *   new_len  [B] int32 out: ctx_len[b] + 1 + accepted_len[b], the processed
+ *            length (the anchor and the accepted drafts); the pending anchor is
+ *            the emitted correction / bonus token.
+ *   keep_pages [B] int32 out (nullable): block-table slots still holding a
+ *            valid position, ceil(new_len / page_size); later slots the block
+ *            wrote may be released.
+ *   status_per_seq [B] int32 out (nullable): SPEC_SEQ_BAD_TREE when
+ *            accepted_len, the path or a page index is out of range; that
+ *            sequence is left untouched and new_len = ctx_len.
+ *   1 <= R <= 64, D in {64, 128}.  Device pointers, async on the stream.
+ * ---------------------------------------------------------------------- */
+spec_status spec_kv_commit(void* k_cache, void* v_cache, int elem_bytes, int num_pages,
+                           int page_size, int Hkv, int D, const int32_t* block_table,
+                           int max_pages, const int32_t* ctx_len, const int32_t* accepted_len,
+                           const int32_t* path, int B, int R, int32_t* new_len,
+                           int32_t* keep_pages, int32_t* status_per_seq, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

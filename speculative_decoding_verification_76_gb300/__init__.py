@@ -5,5 +5,5 @@ include/spec_verify.h); this package is its thin binding plus the seeded
 workload generator used by the tests and the benchmark.
 """
 from .api import (AttnCall, SamplerConfig, SpecError, accept_sample, accept_sample_tree,  # noqa: F401
-                  attn_num_splits, attn_workspace_size, load, new_workspace,
+                  attn_num_splits, attn_workspace_size, kv_commit, load, new_workspace,
                   sample_workspace_size, tree_prepare, verify_attn, workspace_error)

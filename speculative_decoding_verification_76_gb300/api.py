@@ -27,6 +27,7 @@ EXPORTS = (
     "spec_verify_attn_num_splits", "spec_verify_attn", "spec_verify_attn_partials",
     "spec_verify_attn_combine", "spec_accept_sample_workspace_size",
     "spec_accept_sample", "spec_accept_sample_tree", "spec_workspace_error",
+    "spec_kv_commit",
 )
 
 
@@ -98,6 +99,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                             _P]
     lib.spec_workspace_error.restype = _I
     lib.spec_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+    lib.spec_kv_commit.restype = _I
+    lib.spec_kv_commit.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P,
+                                   _P, _P, _P]
     _lib = lib
     return lib
 
@@ -157,6 +161,40 @@ def tree_prepare(parent: torch.Tensor | None, ctx_len: torch.Tensor, R: int | No
                                                       _ptr(anc_mask), _ptr(pos_ids), _ptr(status),
                                                       _stream()))
     return anc_mask, pos_ids, status
+
+
+def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+              ctx_len: torch.Tensor, accepted_len: torch.Tensor, path=None, R: int | None = None,
+              new_len=None, keep_pages=None, status=None):
+    """Processed lengths after acceptance; for a tree (path [B,R] int32) the accepted
+    path's K/V rows are moved in place to positions ctx + 0..accepted_len.
+    Returns (new_len, keep_pages, status)."""
+    lib = load()
+    if k_cache.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("caches must be bf16 or fp32")
+    npg, P, Hkv, D = k_cache.shape
+    _need(k_cache, "k_cache", k_cache.dtype)
+    _need(v_cache, "v_cache", k_cache.dtype, k_cache.shape)
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx_len, "ctx_len", torch.int32)
+    B = ctx_len.shape[0]
+    _need(accepted_len, "accepted_len", torch.int32, (B,))
+    if path is not None:
+        _need(path, "path", torch.int32)
+        R = path.shape[1]
+    if R is None:
+        raise ValueError("R (rows per sequence) is needed for a chain")
+    dev = ctx_len.device
+    new_len = torch.empty((B,), dtype=torch.int32, device=dev) if new_len is None else new_len
+    keep_pages = (torch.empty((B,), dtype=torch.int32, device=dev) if keep_pages is None
+                  else keep_pages)
+    status = torch.empty((B,), dtype=torch.int32, device=dev) if status is None else status
+    _check("spec_kv_commit",
+           lib.spec_kv_commit(_ptr(k_cache), _ptr(v_cache), k_cache.element_size(), npg, P, Hkv,
+                              D, _ptr(block_table), block_table.shape[1], _ptr(ctx_len),
+                              _ptr(accepted_len), _ptr(path), B, R, _ptr(new_len),
+                              _ptr(keep_pages), _ptr(status), _stream()))
+    return new_len, keep_pages, status
 
 
 # ------------------------------------------------------------------ attention

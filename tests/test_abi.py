@@ -112,6 +112,22 @@ def test_workspace_sizes(lib):
     assert sv.sample_workspace_size(4, 64, 128256) >= 256 + 4 * 64 * 16
 
 
+def test_kv_commit_host_validation(lib):
+    # argument errors are refused on the host, before any launch
+    buf = (ctypes.c_int32 * 128)()
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)  # 16-byte aligned host memory
+    assert lib.spec_kv_commit(None, None, 2, 1, 16, 1, 128, p, 1, p, p, None, 1, 8, p, None,
+                              None, None) == api.SPEC_EINVAL
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, 1, 65, p, None, None,
+                              None) == api.SPEC_EINVAL
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 96, p, 1, p, p, None, 1, 8, p, None, None,
+                              None) == api.SPEC_EUNSUPPORTED
+    assert lib.spec_kv_commit(p, p, 3, 1, 16, 1, 128, p, 1, p, p, None, 1, 8, p, None, None,
+                              None) == api.SPEC_EUNSUPPORTED
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, 0, 8, p, None, None,
+                              None) == api.SPEC_OK  # nothing to do
+
+
 def test_split_plan_for_the_bench_shapes(lib):
     # few units: about one wave of CTAs (8B-shaped: 8 KV heads x 17 splits of 512 tokens);
     # units that fill the SMs: 4096-token chunks; explicit counts are honoured
