@@ -17,8 +17,8 @@ def _case(B, R, Hkv, D, P, dtype, seed, tree):
     max_pages = int((ctx.max() + R + P - 1) // P) + 1
     npages = B * max_pages + 3
     table = rng.permutation(npages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
-    k = torch.randn((npages, P, Hkv, D), dtype=torch.float32).to(dtype)
-    v = torch.randn((npages, P, Hkv, D), dtype=torch.float32).to(dtype)
+    k = torch.from_numpy(rng.standard_normal((npages, P, Hkv, D)).astype(np.float32)).to(dtype)
+    v = torch.from_numpy(rng.standard_normal((npages, P, Hkv, D)).astype(np.float32)).to(dtype)
     paths, path = None, None
     if tree:
         parent = np.full((B, R), -1, np.int64)
