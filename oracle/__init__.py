@@ -28,8 +28,12 @@ by eye, with no blocking, fusion or reordering beyond the definitions:
                 compacted into the next logical prefix ("Speculative
                 Decoding" (atlas), "Committed tokens versus cached states",
                 "Chains, trees and visibility").
+  append.py     the block's K/V rows written into the paged cache, keys
+                rotated for their depth position ("Speculative Decoding"
+                (atlas), "Chains, trees and visibility": position ids follow
+                depth; the rotation itself is a reading, see the module).
 
 Every function is pinned by a test in tests/test_oracle_*.py against worked
 examples printed on the pages, closed forms or brute force.
 """
-from . import attention, commit, sampler, tree  # noqa: F401
+from . import append, attention, commit, sampler, tree  # noqa: F401
