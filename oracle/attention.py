@@ -53,6 +53,11 @@ def verify_attention(q, k_cache, v_cache, block_table, ctx_len, anc_mask, scale=
     Returns out [B,R,Hq,D] and lse [B,R,Hq].  batches / rows / heads restrict
     which outputs are computed (the others stay zero); the arithmetic of each
     computed output is unchanged.
+
+    Row i's visible keys are the committed prefix [0, ctx) and the block
+    positions ctx + j with bit j of its mask; the scores, the softmax and the
+    weighted sum run over exactly that set (the query heads that share a KV
+    head are scored together, one column each).
     """
     q = np.asarray(q, dtype=np.float64)
     k_cache = np.asarray(k_cache, dtype=np.float64)
@@ -64,18 +69,24 @@ def verify_attention(q, k_cache, v_cache, block_table, ctx_len, anc_mask, scale=
         scale = 1.0 / math.sqrt(D)
     out = np.zeros((B, R, Hq, D))
     lse = np.zeros((B, R, Hq))
+    hs = list(range(Hq) if heads is None else heads)
     for b in (range(B) if batches is None else batches):
         ctx = int(ctx_len[b])
         K = gather_kv(k_cache, block_table[b], ctx + R)
         Vv = gather_kv(v_cache, block_table[b], ctx + R)
         for i in (range(R) if rows is None else rows):
             vis = visible_positions(ctx, anc_mask[b][i])
-            for h in (range(Hq) if heads is None else heads):
-                kvh = h // G
-                s = K[vis, kvh, :] @ q[b, i, h] * scale
-                smax = s.max()
+            blk = vis[vis >= ctx]                      # the visible block positions
+            for kvh in sorted({h // G for h in hs}):
+                group = [h for h in hs if h // G == kvh]
+                Qg = q[b, i, group, :]                 # [g, D]
+                Kc, Vc = K[:ctx, kvh, :], Vv[:ctx, kvh, :]
+                Kb, Vb = K[blk, kvh, :], Vv[blk, kvh, :]
+                s = np.concatenate([Kc @ Qg.T, Kb @ Qg.T]) * scale   # [n_visible, g]
+                smax = s.max(axis=0)
                 e = np.exp(s - smax)
-                z = e.sum()
-                out[b, i, h] = (e / z) @ Vv[vis, kvh, :]
-                lse[b, i, h] = smax + math.log(z)
+                z = e.sum(axis=0)
+                o = e[:ctx].T @ Vc + e[ctx:].T @ Vb   # sum over the visible set
+                out[b, i, group] = o / z[:, None]
+                lse[b, i, group] = smax + np.log(z)
     return out, lse

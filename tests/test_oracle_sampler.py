@@ -346,3 +346,117 @@ def test_ratio_flag():
     assert r["flagged"]
     r = _walk1(p, q, 1, 0.2, 0.3)
     assert not r["flagged"]
+
+
+# ---------------------------------------------------------------- tree rule: greedy, EOS, zero residual
+# The fox tree as stored (tests/golden/fox_tree.json): fox (anchor) -> {jumps -> {over, high},
+# runs -> {away}}.  Node tokens are arbitrary ids; every expectation below is derived by hand
+# from the stated rules: greedy follows the first child (storage order) whose token is the
+# argmax of the current node's row and emits the argmax at the first mismatch or after a leaf;
+# emission stops after an EOS, whether accepted or emitted as the final token.
+FOX_PARENT = [-1, 0, 1, 1, 0, 4]
+FOX_TOKENS = [-1, 10, 20, 21, 11, 30]          # jumps=10 over=20 high=21 runs=11 away=30
+
+
+def _greedy_rows(argmax_by_row, V=40, N=6):
+    """Logit rows whose argmax is given per row (others: a fixed low pattern)."""
+    logits = np.tile(np.linspace(-1.0, -2.0, V), (N, 1)).astype(np.float32)
+    for r, a in argmax_by_row.items():
+        logits[r, a] = 5.0
+    return logits
+
+
+def _fox_greedy(argmax_by_row, tokens=FOX_TOKENS, eos=-1):
+    cfg = SamplerCfg(greedy=True, eos_id=eos)
+    return osm.accept_tree(_greedy_rows(argmax_by_row), None, tokens, FOX_PARENT, np.zeros(6),
+                           cfg)
+
+
+def test_tree_greedy_walk_fox_by_hand():
+    # fox: argmax 11 = runs (node 4); runs: argmax 30 = away (node 5, a leaf); away: 7
+    r = _fox_greedy({0: 11, 4: 30, 5: 7, 1: 20, 2: 1, 3: 2})
+    assert r["path"] == [4, 5] and r["emitted"] == [11, 30, 7] and r["accepted_len"] == 2
+    # fox: 10 = jumps; jumps: 22 matches neither over (20) nor high (21): emit 22
+    r = _fox_greedy({0: 10, 1: 22})
+    assert r["path"] == [1] and r["emitted"] == [10, 22] and r["accepted_len"] == 1
+    # jumps: 21 = high, the second child (node 3); high is a leaf: its argmax 5 is emitted
+    r = _fox_greedy({0: 10, 1: 21, 3: 5, 2: 9})
+    assert r["path"] == [1, 3] and r["emitted"] == [10, 21, 5]
+    # fox: 12 matches no child: nothing accepted, 12 emitted
+    r = _fox_greedy({0: 12, 1: 20, 4: 30})
+    assert r["path"] == [] and r["emitted"] == [12] and r["accepted_len"] == 0
+
+
+def test_tree_greedy_siblings_with_the_argmax_token():
+    # jumps and runs both carry token 10: the first in storage order (jumps) is followed,
+    # even though only runs' row would have continued the match
+    toks = [-1, 10, 20, 21, 10, 30]
+    r = _fox_greedy({0: 10, 1: 3, 4: 30, 5: 6}, tokens=toks)
+    assert r["path"] == [1] and r["emitted"] == [10, 3]
+    r = _fox_greedy({0: 10, 1: 20, 2: 4}, tokens=toks)
+    assert r["path"] == [1, 2] and r["emitted"] == [10, 20, 4]
+
+
+def test_tree_greedy_eos_on_the_path():
+    # over (20) is EOS and accepted: emission stops there, no bonus after it
+    r = _fox_greedy({0: 10, 1: 20, 2: 5}, eos=20)
+    assert r["path"] == [1, 2] and r["emitted"] == [10, 20] and r["accepted_len"] == 2
+    # the EOS is the correction (matches no child of jumps): emitted last, not accepted
+    r = _fox_greedy({0: 10, 1: 22}, eos=22)
+    assert r["path"] == [1] and r["emitted"] == [10, 22] and r["accepted_len"] == 1
+    # EOS accepted at depth 1 ends the walk before jumps' children are looked at
+    r = _fox_greedy({0: 10, 1: 20}, eos=10)
+    assert r["path"] == [1] and r["emitted"] == [10]
+
+
+def test_tree_walk_eos_stops_after_an_accepted_node():
+    V = 8
+    uni = np.full(V, 1.0 / V)
+    P = [uni] * 6
+    Q = [uni] * 6                         # p = q everywhere: every first child is accepted
+    toks = [-1, 1, 2, 3, 4, 5]
+    u = [0.9, 0.9, 0.9, 0.9, 0.9, 0.3]
+    r = osm.tree_walk(P, Q, toks, FOX_PARENT, u)
+    # fox -> jumps (first child) -> over (first child, a leaf) -> bonus floor(0.3 * 8) = 2
+    assert r["path"] == [1, 2] and r["emitted"] == [1, 2, 2]
+    r = osm.tree_walk(P, Q, toks, FOX_PARENT, u, eos_id=2)
+    assert r["path"] == [1, 2] and r["emitted"] == [1, 2] and r["accepted_len"] == 2
+    r = osm.tree_walk(P, Q, toks, FOX_PARENT, u, eos_id=1)
+    assert r["path"] == [1] and r["emitted"] == [1]
+
+
+def test_zero_residual_draws_from_p_chain_and_tree():
+    # p = q and the proposal has p = q = 0: it is rejected (u * 0 < 0 is false) and the
+    # positive part of p - q is empty, so the draw falls back to p (reported, flagged)
+    p = np.array([0.5, 0.5, 0.0, 0.0])
+    r = osm.chain_walk([p, p], [p], [2], [0.5, 0.3])
+    assert r["accepted_len"] == 0 and r["emitted"] == [0]      # 0.3 * 1 < 0.5: token 0
+    assert r["status"] & osm.ST_RESID_ZERO and r["status"] & osm.ST_QZERO and r["flagged"]
+    r = osm.chain_walk([p, p], [p], [3], [0.5, 0.7])
+    assert r["emitted"] == [1]
+    # tree: both children of fox propose a zero-mass token; p' stays p_root throughout
+    toks = [-1, 2, 20, 21, 3, 30]
+    P = [p] * 6
+    Q = [p] * 6
+    r = osm.tree_walk(P, Q, toks, FOX_PARENT, [0.5, 0.5, 0.5, 0.5, 0.5, 0.7])
+    assert r["path"] == [] and r["emitted"] == [1]
+    assert r["status"] & osm.ST_RESID_ZERO and r["flagged"]
+
+
+def test_tree_topp_ambiguity_flags_only_when_outcome_changes():
+    # the anchor's row has a top-p cutoff on the boundary between 2 and 3 kept tokens
+    logits_root = np.log(np.array([0.4, 0.3, 0.2, 0.1])).astype(np.float32)
+    logits_leaf = np.log(np.array([0.97, 0.01, 0.01, 0.01])).astype(np.float32)
+    cfg = SamplerCfg(top_p=0.7)
+    q = np.full((2, 4), 0.25)
+    parent = [-1, 0]
+    logits = np.stack([logits_root, logits_leaf])
+    # token 0 is accepted under either cutoff (p(0) >= 0.4 / 0.9 > q): robust
+    rob = osm.accept_tree(logits, q, [-1, 0], parent, [0.5, 0.1], cfg)
+    assert rob["path"] == [1] and not rob["flagged"]
+    # token 2 is kept only by the 3-token cutoff: the walk depends on it
+    amb = osm.accept_tree(logits, q, [-1, 2], parent, [0.5, 0.1], cfg)
+    assert amb["flagged"]
+    # the same rows without ambiguity (top_p clear of the boundary) are not flagged
+    clear = osm.accept_tree(logits, q, [-1, 2], parent, [0.5, 0.1], SamplerCfg(top_p=0.85))
+    assert not clear["flagged"] and clear["path"] == [1]
