@@ -182,7 +182,13 @@ spec_status spec_verify_attn_combine(const void* q, const void* k_cache, const v
  *     there.  Calls whose GPU work overlaps (different streams, or different
  *     host threads on one device without ordering) race on it and give wrong
  *     results: order them on one stream.
- *   - Results equal spec_verify_attn's for the same arguments.
+ *   - The cached address belongs to the device's current context: calls must
+ *     not span a reset of the device (cudaDeviceReset).
+ *   - Outputs equal spec_verify_attn's for the same arguments.  A bounded
+ *     device wait that runs out is recorded in an error word at the head of
+ *     the fixed array, which each call clears when it starts; read it with
+ *     spec_verify_attn_noalloc_error after the call (the outputs of a call
+ *     whose word is nonzero are unspecified, as for spec_verify_attn).
  * ---------------------------------------------------------------------- */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -192,6 +198,11 @@ spec_status spec_verify_attn_noalloc(const void* q, const void* k_cache, const v
                                      const int32_t* ctx_len, const uint64_t* anc_mask,
                                      int B, int R, int Hq, int Hkv, int D, float scale,
                                      int num_splits, void* out, float* lse_out, void* stream);
+
+/* The error word of the last spec_verify_attn_noalloc call on the current
+ * device (0, or SPEC_ERR_MBAR_TIMEOUT), copied to *host_err.  Synchronises
+ * `stream`, on which that call was enqueued; allocates nothing. */
+spec_status spec_verify_attn_noalloc_error(int32_t* host_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Sampler settings, as actually served ("Greedy, sampling and the real
@@ -287,10 +298,18 @@ spec_status spec_workspace_error(const void* workspace, int32_t* host_err, void*
  *   block_table [B, max_pages] int32; ctx_len [B] int32: block row j was
  *            written at cache position ctx_len[b] + j.
  *   accepted_len [B] int32: drafts accepted (0 .. R-1).
- *   path     [B, R] int32 (NULL: a chain, nothing moves): node 0 then the
- *            accepted nodes in order (entries past accepted_len[b] ignored);
- *            node ids strictly increase.  The K/V rows of path[b][k] move to
- *            position ctx_len[b] + k (every row is read before any is written).
+ *   path     [B, R] int32 (NULL: a chain, nothing moves): the accepted nodes
+ *            in order, exactly as spec_accept_sample_tree writes path_nodes
+ *            (node 0, the anchor, is implied and not listed; entries past
+ *            accepted_len[b] are ignored).  Node ids must strictly increase
+ *            (a tree in storage order puts a child after its parent).  The
+ *            K/V rows of path[b][k] move to position ctx_len[b] + k + 1; node
+ *            0 stays at ctx_len[b].  Every row is read before any is written.
+ *   parent   [B, R] int32 (nullable; only with path): the tree's parent
+ *            array; when given, each path node must be a child of the one
+ *            before it (the first a child of node 0).  Without it only the
+ *            order is checked and the caller must pass a real root-to-node
+ *            path: the compacted keys keep the rotation of their depth.
  *   new_len  [B] int32 out: ctx_len[b] + 1 + accepted_len[b], the processed
  *            length (the anchor and the accepted drafts); the pending anchor is
  *            the emitted correction / bonus token.
@@ -298,14 +317,16 @@ spec_status spec_workspace_error(const void* workspace, int32_t* host_err, void*
  *            valid position, ceil(new_len / page_size); later slots the block
  *            wrote may be released.
  *   status_per_seq [B] int32 out (nullable): SPEC_SEQ_BAD_TREE when
- *            accepted_len, the path or a page index is out of range; that
- *            sequence is left untouched and new_len = ctx_len.
+ *            accepted_len, the path or a page index it touches is out of
+ *            range, or the path breaks the rules above; that sequence is left
+ *            untouched and new_len = ctx_len.
  *   1 <= R <= 64, D in {64, 128}.  Device pointers, async on the stream.
  * ---------------------------------------------------------------------- */
 spec_status spec_kv_commit(void* k_cache, void* v_cache, int elem_bytes, int num_pages,
                            int page_size, int Hkv, int D, const int32_t* block_table,
                            int max_pages, const int32_t* ctx_len, const int32_t* accepted_len,
-                           const int32_t* path, int B, int R, int32_t* new_len,
+                           const int32_t* path, const int32_t* parent, int B, int R,
+                           int32_t* new_len,
                            int32_t* keep_pages, int32_t* status_per_seq, void* stream);
 
 #ifdef __cplusplus

@@ -27,7 +27,7 @@ EXPORTS = (
     "spec_verify_attn_num_splits", "spec_verify_attn", "spec_verify_attn_partials",
     "spec_verify_attn_combine", "spec_accept_sample_workspace_size",
     "spec_accept_sample", "spec_accept_sample_tree", "spec_workspace_error",
-    "spec_kv_commit",
+    "spec_kv_commit", "spec_verify_attn_noalloc", "spec_verify_attn_noalloc_error",
 )
 
 
@@ -100,8 +100,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_workspace_error.restype = _I
     lib.spec_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
     lib.spec_kv_commit.restype = _I
-    lib.spec_kv_commit.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P,
-                                   _P, _P, _P]
+    lib.spec_kv_commit.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I,
+                                   _P, _P, _P, _P]
+    lib.spec_verify_attn_noalloc.restype = _I
+    lib.spec_verify_attn_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _I, _I, _I,
+                                             _I, _I, ctypes.c_float, _I, _P, _P, _P]
+    lib.spec_verify_attn_noalloc_error.restype = _I
+    lib.spec_verify_attn_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
     _lib = lib
     return lib
 
@@ -164,10 +169,12 @@ def tree_prepare(parent: torch.Tensor | None, ctx_len: torch.Tensor, R: int | No
 
 
 def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
-              ctx_len: torch.Tensor, accepted_len: torch.Tensor, path=None, R: int | None = None,
-              new_len=None, keep_pages=None, status=None):
-    """Processed lengths after acceptance; for a tree (path [B,R] int32) the accepted
-    path's K/V rows are moved in place to positions ctx + 0..accepted_len.
+              ctx_len: torch.Tensor, accepted_len: torch.Tensor, path=None, parent=None,
+              R: int | None = None, new_len=None, keep_pages=None, status=None, stream=None):
+    """Processed lengths after acceptance.  For a tree, path [B,R] int32 holds the
+    accepted nodes (node 0 implied), as accept_sample_tree returns them; their K/V
+    rows move in place to positions ctx + 1 .. ctx + accepted_len.  parent [B,R]
+    (optional) lets the kernel check that the path follows the tree.
     Returns (new_len, keep_pages, status)."""
     lib = load()
     if k_cache.dtype not in (torch.bfloat16, torch.float32):
@@ -182,6 +189,8 @@ def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.T
     if path is not None:
         _need(path, "path", torch.int32)
         R = path.shape[1]
+    if parent is not None:
+        _need(parent, "parent", torch.int32, (B, R))
     if R is None:
         raise ValueError("R (rows per sequence) is needed for a chain")
     dev = ctx_len.device
@@ -192,8 +201,8 @@ def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.T
     _check("spec_kv_commit",
            lib.spec_kv_commit(_ptr(k_cache), _ptr(v_cache), k_cache.element_size(), npg, P, Hkv,
                               D, _ptr(block_table), block_table.shape[1], _ptr(ctx_len),
-                              _ptr(accepted_len), _ptr(path), B, R, _ptr(new_len),
-                              _ptr(keep_pages), _ptr(status), _stream()))
+                              _ptr(accepted_len), _ptr(path), _ptr(parent), B, R, _ptr(new_len),
+                              _ptr(keep_pages), _ptr(status), _stream(stream)))
     return new_len, keep_pages, status
 
 

@@ -22,7 +22,6 @@
 // token groups take alternate stages and merge through shared memory at
 // the end.  An fp32 CUDA-core kernel serves fp32 caches.
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -646,13 +645,9 @@ size_t smem_bytes_bf16(int NRG, int stages, int stage_tok) {
 template <int NRG>
 spec_status launch_bf16(const AttnParams& prm, const Plan& pl, cudaStream_t st) {
   const size_t smem = smem_bytes_bf16(NRG, stages_for<NRG>(), stage_tokens<NRG>());
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_partial_bf16<NRG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return SPEC_ECUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce<int> smem_once;  // once per device
+  const spec_status ra = ensure_smem_limit(smem_once, (const void*)attn_partial_bf16<NRG>, (int)smem);
+  if (ra != SPEC_OK) return ra;
   dim3 grid(prm.Hkv * pl.row_tiles, pl.S, prm.B);
   attn_partial_bf16<NRG><<<grid, kThreads, smem, st>>>(prm);
   return launch_status();
@@ -803,25 +798,24 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+PerDeviceOnce<void*> g_noalloc_addr;
 
 // Device address of g_noalloc_scratch on the current device.  The first call
 // on a device looks it up (cudaGetSymbolAddress, with that device current);
-// later calls reuse the cached address.  No memory is allocated.
+// later calls reuse the cached address.  No memory is allocated.  The cache
+// is keyed by device ordinal, so calls must not span a reset of the device
+// (cudaDeviceReset), after which the cached address is stale.
 spec_status noalloc_scratch(void** addr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ECUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return SPEC_EUNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ECUDA;
-    g_noalloc_addr[dev] = p;
-  }
-  *addr = g_noalloc_addr[dev];
-  return SPEC_OK;
+  const int rc = g_noalloc_addr.run(
+      dev,
+      [](void** p) {
+        return (cudaGetSymbolAddress(p, g_noalloc_scratch) == cudaSuccess && *p) ? 0 : 1;
+      },
+      addr);
+  if (rc == -1) return SPEC_EUNSUPPORTED;
+  return rc == 0 ? SPEC_OK : SPEC_ECUDA;
 }
 
 }  // namespace
@@ -850,4 +844,20 @@ extern "C" spec_status spec_verify_attn_noalloc(const void* q, const void* k_cac
   return verify_attn_impl(q, k_cache, v_cache, dtype, page_size, num_pages, block_table,
                           max_pages, ctx_len, anc_mask, B, R, Hq, Hkv, D, scale, num_splits,
                           scratch, SPEC_NOALLOC_SCRATCH_BYTES, out, lse_out, stream, kBoth);
+}
+
+// The error word of the allocation-free call's scratch (the head of the
+// fixed array), for callers that cannot address that array themselves.
+// Reads it with a copy from the symbol on `stream`, then waits for the
+// stream; allocates nothing.
+extern "C" spec_status spec_verify_attn_noalloc_error(int32_t* host_err, void* stream) {
+  if (!host_err) return SPEC_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_noalloc_scratch, sizeof(int32_t), 0, cudaMemcpyDeviceToHost,
+                                st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SPEC_ECUDA;
+  *host_err = v;
+  return SPEC_OK;
 }

@@ -1,6 +1,6 @@
 // Shared device helpers for libspecverify (sm_103a).  Inline PTX wrappers for
-// mbarrier, TMA, thread-block clusters / distributed shared memory and the
-// warp-level MMA used by the attention kernel.
+// mbarrier, bulk copies, thread-block clusters / distributed shared memory and
+// the warp-level MMA; the host-side per-device setup helper.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "../../include/spec_verify.h"
+#include "dev_once.h"
 
 #define SPEC_DEV __device__ __forceinline__
 
@@ -101,22 +102,7 @@ SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   return false;
 }
 
-// ---------------------------------------------------------------- TMA
-// 3-D tiled load (x = innermost element coordinate) into shared memory,
-// completion counted on an mbarrier.
-SPEC_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                          int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-SPEC_DEV void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
+// ---------------------------------------------------------------- bulk copies
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
 SPEC_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -124,13 +110,6 @@ SPEC_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64
           "r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Warm [gsrc, gsrc + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
-SPEC_DEV void prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)),
-               "r"(bytes)
-               : "memory");
 }
 
 // ---------------------------------------------------------------- clusters
@@ -243,4 +222,21 @@ SPEC_DEV float warp_sum(float v) {
 
 static inline spec_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+// Raise `func`'s dynamic shared-memory limit to `bytes` on the current device,
+// once per device and thread-safely (`once` is the launch site's record).
+// Device ordinals beyond the record's range set the attribute on every call.
+static inline spec_status ensure_smem_limit(PerDeviceOnce<int>& once, const void* func, int bytes) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ECUDA;
+  auto set = [&](int*) {
+    return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+                   cudaSuccess
+               ? 0
+               : 1;
+  };
+  const int rc = once.run(dev, set);
+  if (rc == -1) return set(nullptr) == 0 ? SPEC_OK : SPEC_ECUDA;
+  return rc == 0 ? SPEC_OK : SPEC_ECUDA;
 }

@@ -2384,13 +2384,11 @@ size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
 
 template <int NT, bool FAST, bool TR>
 spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t st) {
-  static bool attr_set = false;  // once, at the largest size, so graph captures need no setup
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_kernel<NT, FAST, TR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dyn_smem(kMaxSliceBytes, true)) != cudaSuccess)
-      return SPEC_ECUDA;
-    attr_set = true;
-  }
+  // once per device, at the largest size, so graph captures need no setup
+  static PerDeviceOnce<int> smem_once;
+  const spec_status ra = ensure_smem_limit(smem_once, (const void*)sampler_kernel<NT, FAST, TR>,
+                                           (int)dyn_smem(kMaxSliceBytes, true));
+  if (ra != SPEC_OK) return ra;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(pl.CS * rows), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
@@ -2414,13 +2412,10 @@ size_t stream_smem(int V) {
 
 template <bool FAST>
 spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(sampler_stream_kernel<FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem(kSListMaxV)) != cudaSuccess)
-      return SPEC_ECUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce<int> smem_once;  // once per device, at the largest size
+  const spec_status ra = ensure_smem_limit(smem_once, (const void*)sampler_stream_kernel<FAST>,
+                                           (int)stream_smem(kSListMaxV));
+  if (ra != SPEC_OK) return ra;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows, 1, 1);
   cfg.blockDim = dim3(kSNT, 1, 1);

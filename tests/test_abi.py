@@ -116,15 +116,18 @@ def test_kv_commit_host_validation(lib):
     # argument errors are refused on the host, before any launch
     buf = (ctypes.c_int32 * 128)()
     p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)  # 16-byte aligned host memory
-    assert lib.spec_kv_commit(None, None, 2, 1, 16, 1, 128, p, 1, p, p, None, 1, 8, p, None,
+    assert lib.spec_kv_commit(None, None, 2, 1, 16, 1, 128, p, 1, p, p, None, None, 1, 8, p,
+                              None, None, None) == api.SPEC_EINVAL
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, None, 1, 65, p, None,
                               None, None) == api.SPEC_EINVAL
-    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, 1, 65, p, None, None,
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 96, p, 1, p, p, None, None, 1, 8, p, None, None,
+                              None) == api.SPEC_EUNSUPPORTED
+    assert lib.spec_kv_commit(p, p, 3, 1, 16, 1, 128, p, 1, p, p, None, None, 1, 8, p, None, None,
+                              None) == api.SPEC_EUNSUPPORTED
+    # a parent array without a path has nothing to check
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, p, 1, 8, p, None, None,
                               None) == api.SPEC_EINVAL
-    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 96, p, 1, p, p, None, 1, 8, p, None, None,
-                              None) == api.SPEC_EUNSUPPORTED
-    assert lib.spec_kv_commit(p, p, 3, 1, 16, 1, 128, p, 1, p, p, None, 1, 8, p, None, None,
-                              None) == api.SPEC_EUNSUPPORTED
-    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, 0, 8, p, None, None,
+    assert lib.spec_kv_commit(p, p, 2, 1, 16, 1, 128, p, 1, p, p, None, None, 0, 8, p, None, None,
                               None) == api.SPEC_OK  # nothing to do
 
 
@@ -135,6 +138,16 @@ def test_split_plan_for_the_bench_shapes(lib):
     assert sv.attn_num_splits(64, 5, 32, 8, 128, 16, 1025) == 5  # 16400 tokens / 4096
     assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193) == 33  # 131088 tokens / 4096
     assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193, 128) >= 128
+
+
+def test_noalloc_host_checks(lib):
+    # a null output for the error reader, and sizes refused before any device work
+    assert lib.spec_verify_attn_noalloc_error(None, None) == api.SPEC_EINVAL
+    p = ctypes.c_void_p(4096)
+    assert lib.spec_verify_attn_noalloc(p, p, p, api.SPEC_BF16, 16, 10, p, 4, p, p, -1, 4, 8, 2,
+                                        128, 0.0, 0, p, None, None) == api.SPEC_EINVAL
+    assert lib.spec_verify_attn_noalloc(p, p, p, api.SPEC_BF16, 16, 10, p, 4, p, p, 0, 4, 8, 2,
+                                        128, 0.0, 0, p, None, None) == api.SPEC_OK
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

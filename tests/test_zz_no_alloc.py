@@ -6,7 +6,8 @@ serving loop whose memory is fixed after start-up): its scratch is a fixed
 array inside the library.  These tests check that it returns what the
 workspace-based spec_verify_attn returns, on two calls in a row with
 different problems (the shared array keeps the previous call's contents),
-and that a problem too big for the array is refused before any launch.
+that the call's error word (read with spec_verify_attn_noalloc_error) stays
+zero, and that a problem too big for the array is refused before any launch.
 This file is collected last on purpose.
 """
 import ctypes
@@ -63,6 +64,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
         out = torch.full_like(w.q, float("nan"))
         lse = torch.full(ref_lse.shape, float("nan"), device=DEV)
         assert _call(f, w, anc, out, lse) == api.SPEC_OK
+        # the call's error word, read without allocating: no bounded wait ran out
+        err = ctypes.c_int32(-1)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert sv.load().spec_verify_attn_noalloc_error(ctypes.byref(err), stream) == api.SPEC_OK
+        assert err.value == 0
         torch.cuda.synchronize()
         np.testing.assert_allclose(out.float().cpu().numpy(), ref_out.float().cpu().numpy(),
                                    rtol=0, atol=BF16_ATOL)
