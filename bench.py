@@ -9,15 +9,18 @@ log-sum-exp combine) and the acceptance sampler.  Prints ONE JSON line.
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
 
 Timing: inputs resident in HBM; the step is captured once in a CUDA graph
-and replayed; L2 is flushed before every timed step, outside the timed
-events: a 2 x L2-size write, then a 2 x L2-size read of another buffer so that
-the flush leaves no dirty lines whose write-back would land inside the step;
-each step is timed with CUDA events on its stream; K steps are bracketed by a
-barrier + synchronize; the max over ranks is reported.  The dominant kernel
-(the split-K partial pass) is timed with its own events inside the captured
-step for the roofline entry.
+(attention on the launching stream, the sampler on a second stream forked and
+joined inside the graph: the two share no inputs) and replayed; L2 is flushed
+before every timed step, outside the timed events: a 2 x L2-size write, then a
+2 x L2-size read of another buffer so that the flush leaves no dirty lines whose
+write-back would land inside the step; each step is timed with CUDA events on
+its stream; K steps are bracketed by a barrier + synchronize; the max over ranks
+is reported.  The partial pass and the sampler are timed with their own events
+inside the captured step.  The other configurations are timed the same way and
+reported under "per_workload".
 """
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import os
@@ -26,7 +29,7 @@ import subprocess
 import sys
 import time
 
-os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle leg runs on one core
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle legs: one core per thread
 os.environ.setdefault("OMP_NUM_THREADS", "1")
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -39,9 +42,11 @@ from speculative_decoding_verification_76_gb300 import workloads as wl  # noqa: 
 
 METRIC = "verified positions/sec and achieved HBM GB/s (fraction of roofline), 1×GB300"
 UNIT = "positions/s"
-DEFAULT_WORKLOAD = "llama8b_chain"
+DEFAULT_WORKLOAD = "batched_serving_a75"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+# the attention kernel sources an ncu traffic record must have been taken on
+TRAFFIC_SOURCES = ("attn.cu", "attn_tc.cu", "common.cuh", "tc_ptx.cuh")
 
 
 # ------------------------------------------------------------------ helpers
@@ -92,12 +97,23 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
 
 
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured burst (MEASURED_PEAKS.json bf16_tflops)"
+    except (OSError, ValueError, KeyError):
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "speculative_decoding_verification_76_gb300", "csrc", f),
-                  "rb") as fh:
-            h.update(fh.read())
+    for f in TRAFFIC_SOURCES:
+        p = os.path.join(ROOT, "speculative_decoding_verification_76_gb300", "csrc", f)
+        if os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -114,6 +130,10 @@ def recorded_traffic(workload: str):
     except (OSError, ValueError, KeyError):
         pass
     return None
+
+
+def pct(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
 
 
 class ClockSampler:
@@ -172,7 +192,7 @@ class ClockSampler:
 class GpuStep:
     """All buffers of one verify step, resident on the device."""
 
-    def __init__(self, spec: wl.Spec, device, seed=None):
+    def __init__(self, spec: wl.Spec, device, seed=None, overlap=True):
         import speculative_decoding_verification_76_gb300 as sv
         self.sv = sv
         self.spec = spec
@@ -193,18 +213,14 @@ class GpuStep:
                          status=torch.empty(B, dtype=torch.int32, device=device))
         if spec.is_tree:
             self.sout["path"] = torch.empty((B, R), dtype=torch.int32, device=device)
-        self.ev = None
+        self.overlap = overlap
+        self.side = torch.cuda.Stream(device=device)
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
         self.launches_per_step = 4
 
-    def run(self, ev=None):
+    def sample(self):
         sv, w = self.sv, self.w
-        sv.tree_prepare(w.parent, w.ctx_len, anc_mask=self.anc, pos_ids=self.pos, status=self.tst)
-        if ev is not None:
-            ev[0].record()
-        self.attn.partials()
-        if ev is not None:
-            ev[1].record()
-        self.attn.combine()
         if self.spec.is_tree:
             sv.accept_sample_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms,
                                   self.cfg, workspace=self.sws, out=self.sout)
@@ -213,46 +229,73 @@ class GpuStep:
                              w.draft_tokens, w.uniforms, self.cfg, workspace=self.sws,
                              out=self.sout)
 
+    def run(self, ev=None):
+        """One step.  ev: 4 events (partial start/end, sampler start/end) or None."""
+        sv, w = self.sv, self.w
+        main = torch.cuda.current_stream()
+        if self.overlap:            # the sampler on a second stream, joined below
+            self.fork.record(main)
+            self.side.wait_event(self.fork)
+            with torch.cuda.stream(self.side):
+                if ev is not None:
+                    ev[2].record(self.side)
+                self.sample()
+                if ev is not None:
+                    ev[3].record(self.side)
+            self.join.record(self.side)
+        sv.tree_prepare(w.parent, w.ctx_len, anc_mask=self.anc, pos_ids=self.pos, status=self.tst)
+        if ev is not None:
+            ev[0].record(main)
+        self.attn.partials()
+        if ev is not None:
+            ev[1].record(main)
+        self.attn.combine()
+        if self.overlap:
+            main.wait_event(self.join)
+        else:
+            if ev is not None:
+                ev[2].record(main)
+            self.sample()
+            if ev is not None:
+                ev[3].record(main)
 
-def bench_gpu(args, spec, ws, rank, local):
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    import speculative_decoding_verification_76_gb300 as sv
-    sv.load()
-    step = GpuStep(spec, dev)
-    ctx = step.w.ctx_len.cpu().numpy()
-    nbytes = wl.algorithmic_bytes(spec, ctx)
+
+def make_flusher(dev):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
 
     def flush_l2():
         flush.zero_()           # evict the inputs: write more than L2 holds
         clean.sum()             # then read more than L2 holds: write-backs finish here
-    stream = torch.cuda.current_stream()
+    return flush_l2
 
+
+def time_step(step: GpuStep, steps: int, warmup: int, flush_l2, ws: int, gpu_index=None):
+    """Capture the step in a graph and time `steps` replays (L2 flushed before each)."""
+    stream = torch.cuda.current_stream()
     for _ in range(3):                     # eager warm-up: attributes, descriptors
         step.run()
     torch.cuda.synchronize()
-    try:   # events captured as graph nodes time the partial kernel inside each replay
-        ev_in = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    try:   # events captured as graph nodes time the partial pass and the sampler
+        ev_in = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
     except TypeError:
         ev_in = None
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step.run(ev_in)
     torch.cuda.synchronize()
-
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, part_ms = [], []
-    with ClockSampler(gpu_index) as clk:
-        for _ in range(args.warmup):
+    step_ms, part_ms, samp_ms = [], [], []
+    clk = ClockSampler(gpu_index) if gpu_index is not None else None
+    if clk:
+        clk.__enter__()
+    try:
+        for _ in range(warmup):
             flush_l2()
             graph.replay()
         barrier(ws)
         torch.cuda.synchronize()
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush_l2()
             e0.record(stream)
             graph.replay()
@@ -261,57 +304,140 @@ def bench_gpu(args, spec, ws, rank, local):
             step_ms.append(e0.elapsed_time(e1))
             if ev_in is not None:
                 part_ms.append(ev_in[0].elapsed_time(ev_in[1]))
+                samp_ms.append(ev_in[2].elapsed_time(ev_in[3]))
         torch.cuda.synchronize()
         barrier(ws)
-        if ev_in is None:   # no graph event nodes: time the partial pass eagerly
-            for _ in range(min(args.steps, 200)):
-                flush_l2()
-                e0.record(stream)
-                step.attn.partials()
-                e1.record(stream)
-                e1.synchronize()
-                part_ms.append(e0.elapsed_time(e1))
-    clocks = clk.summary()
-    err = sv.workspace_error(step.attn.workspace) | sv.workspace_error(step.sws)
+    finally:
+        if clk:
+            clk.__exit__()
+    if ev_in is None:   # no graph event nodes: time the partial pass eagerly
+        for _ in range(min(steps, 200)):
+            flush_l2()
+            e0.record(stream)
+            step.attn.partials()
+            e1.record(stream)
+            e1.synchronize()
+            part_ms.append(e0.elapsed_time(e1))
+    err = step.sv.workspace_error(step.attn.workspace) | step.sv.workspace_error(step.sws)
     if err:
         raise RuntimeError(f"device wait timed out (error word {err:#x})")
+    return {"step_ms": step_ms, "part_ms": part_ms, "samp_ms": samp_ms,
+            "clocks": clk.summary() if clk else None}
 
-    mean_ms = statistics.fmean(step_ms)
-    mean_ms_all = max_over_ranks(mean_ms, ws, device=dev)
-    positions = spec.B * spec.R
-    total_positions = sum_over_ranks(positions, ws, device=dev)
-    value = total_positions / (mean_ms_all * 1e-3)
-    part_mean = statistics.fmean(part_ms)
-    peak, peak_src = hbm_peak()
-    attn_gbs = nbytes["attn"] / (part_mean * 1e-3) / 1e9
-    step_gbs = nbytes["step"] / (mean_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(spec.name)
 
-    acc = step.sout["accepted_len"].cpu().numpy()
-    e2e = bench_e2e(step, spec, max(3, min(args.steps, 50)), ws, dev)
-    out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": arm_config(spec, int(ctx.max()), ws),
+def acceptance_stats(spec, acc: np.ndarray):
+    """Accepted-length histogram over all sequences and the empirical acceptance
+    rate of each draft position (accepted / reached)."""
+    acc = np.asarray(acc)
+    hist = np.bincount(np.clip(acc, 0, None), minlength=spec.R).tolist()
+    out = {"accepted_len_hist": hist, "mean_accepted": float(acc.mean()),
+           "mean_emitted": float(acc.mean() + 1)}
+    if not spec.is_tree:
+        alpha = []
+        for i in range(1, spec.R):
+            reached = int((acc >= i - 1).sum())
+            alpha.append(float((acc >= i).sum()) / reached if reached else None)
+        out["alpha_per_position"] = alpha
+    return out
+
+
+def step_record(spec, step, t, nbytes, peak, ws, dev):
+    """Throughput, fractions and timing statistics of one timed workload."""
+    ms = t["step_ms"]
+    mean_ms = statistics.fmean(ms)
+    mean_all = max_over_ranks(mean_ms, ws, device=dev)
+    med = statistics.median(ms)
+    part = statistics.fmean(t["part_ms"])
+    rec = {
+        "ms_mean": mean_all, "ms_median": med, "ms_p10": pct(ms, 10), "ms_p90": pct(ms, 90),
+        "positions_per_s": sum_over_ranks(spec.B * spec.R, ws, device=dev) / (mean_all * 1e-3),
+        "sequences_per_s": sum_over_ranks(spec.B, ws, device=dev) / (mean_all * 1e-3),
+        "step_bytes": nbytes["step"], "step_bytes_all_q_rows": nbytes["step_all_q"],
+        "step_hbm_frac": nbytes["step"] / (med * 1e-3) / 1e9 / peak,
+        "step_hbm_frac_all_q_rows": nbytes["step_all_q"] / (med * 1e-3) / 1e9 / peak,
+        "attn_partial_us": part * 1e3,
+        "attn_partial_frac": nbytes["attn"] / (part * 1e-3) / 1e9 / peak,
+        "sampler_us": statistics.fmean(t["samp_ms"]) * 1e3 if t["samp_ms"] else None,
         "attn_num_splits": step.sv.attn_num_splits(
             spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
             step.w.block_table.shape[1], spec.num_splits),
-        "sequences_per_s": sum_over_ranks(spec.B, ws, device=dev) / (mean_ms_all * 1e-3),
-        "step_hbm_gbs": step_gbs, "step_hbm_frac": step_gbs / peak,
-        "step_algorithmic_bytes": nbytes["step"],
-        "roofline": {"bound": "hbm", "kernel": "attn_partial_bf16 (split-K partials)",
+    }
+    if spec.is_tree or spec.R * spec.Hq // spec.Hkv >= 128:
+        # a contraction-heavy shape: also against the bf16 tensor peak
+        ctx = step.w.ctx_len.cpu().numpy().astype(np.float64)
+        flop = 4.0 * spec.D * spec.Hq * spec.R * float(np.sum(ctx + spec.R))
+        tpk, _ = bf16_peak()
+        rec["attn_partial_tflops"] = flop / (part * 1e-3) / 1e12
+        rec["attn_partial_tensor_frac"] = rec["attn_partial_tflops"] / tpk
+    return rec
+
+
+def bench_gpu(args, spec, ws, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_verification_76_gb300 as sv
+    sv.load()
+    flush_l2 = make_flusher(dev)
+    step = GpuStep(spec, dev, overlap=not args.serial)
+    ctx = step.w.ctx_len.cpu().numpy()
+    nbytes = wl.algorithmic_bytes(spec, ctx)
+    peak, peak_src = hbm_peak()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    t = time_step(step, args.steps, args.warmup, flush_l2, ws, gpu_index)
+    rec = step_record(spec, step, t, nbytes, peak, ws, dev)
+    part_mean = rec["attn_partial_us"] * 1e-6
+    attn_gbs = nbytes["attn"] / part_mean / 1e9
+    traffic = recorded_traffic(spec.name)
+    acc = step.sout["accepted_len"].cpu().numpy()
+    e2e = bench_e2e(step, spec, max(3, min(args.steps, 50)), ws, dev)
+    out = {
+        "metric": METRIC, "value": rec["positions_per_s"], "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_mean"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": arm_config(spec, int(ctx.max()), ws),
+        "ms_median": rec["ms_median"], "ms_p10": rec["ms_p10"], "ms_p90": rec["ms_p90"],
+        "sequences_per_s": rec["sequences_per_s"],
+        "step_hbm_gbs": nbytes["step"] / (rec["ms_median"] * 1e-3) / 1e9,
+        "step_hbm_frac": rec["step_hbm_frac"], "step_algorithmic_bytes": nbytes["step"],
+        "step_hbm_frac_all_q_rows": rec["step_hbm_frac_all_q_rows"],
+        "step_algorithmic_bytes_all_q_rows": nbytes["step_all_q"],
+        "attn_num_splits": rec["attn_num_splits"], "sampler_us": rec["sampler_us"],
+        "roofline": {"bound": "hbm", "kernel": "attention partial pass (split-K)",
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": traffic,
-                     "algorithmic_bytes": nbytes["attn"], "mean_launch_us": part_mean * 1e3,
+                     "algorithmic_bytes": nbytes["attn"], "mean_launch_us": part_mean * 1e6,
                      "peak_source": peak_src},
-        "accepted_len_hist": np.bincount(np.clip(acc, 0, None),
-                                         minlength=spec.R).tolist(),
+        **acceptance_stats(spec, acc),
         "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps,
-        "clocks": clocks,
+        "clocks": t["clocks"],
     }
+    if not args.no_per_workload:
+        del step
+        torch.cuda.empty_cache()
+        out["per_workload"] = per_workload(args, spec, ws, dev, flush_l2, peak)
     return out
+
+
+def per_workload(args, headline, ws, dev, flush_l2, peak):
+    """The other configurations (the tiny one is a parity case only), each in its
+    own graph, timed like the headline."""
+    res = {}
+    for name, spec in wl.SPECS.items():
+        if name in (headline.name, "tiny_chain"):
+            continue
+        step = GpuStep(spec, dev, overlap=not args.serial)
+        ctx = step.w.ctx_len.cpu().numpy()
+        nbytes = wl.algorithmic_bytes(spec, ctx)
+        t = time_step(step, args.per_workload_steps, args.warmup, flush_l2, ws)
+        rec = step_record(spec, step, t, nbytes, peak, ws, dev)
+        rec.update(acceptance_stats(spec, step.sout["accepted_len"].cpu().numpy()))
+        res[name] = rec
+        del step
+        torch.cuda.empty_cache()
+    return res
 
 
 def arm_config(spec, seq_len, ws):
@@ -321,7 +447,7 @@ def arm_config(spec, seq_len, ws):
         "rows_per_seq": spec.R, "tree": spec.is_tree, "q_heads": spec.Hq,
         "kv_heads": spec.Hkv, "head_dim": spec.D, "vocab": spec.V, "page_size": spec.page_size,
         "temperature": spec.temperature, "top_k": spec.top_k, "top_p": spec.top_p,
-        "greedy": spec.greedy, "parallelism": f"replicas{ws}",
+        "greedy": spec.greedy, "draft_noise": spec.draft_noise, "parallelism": f"replicas{ws}",
         "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read of a second "
               "buffer; outside the timed events)",
         "timing": "CUDA-graph replay, CUDA events per step"}
@@ -413,8 +539,7 @@ def oracle_step(spec, w, heads, batches):
     return (t_attn * spec.Hq / heads + t_samp) * scale_b
 
 
-def cpu_baseline(spec, budget_s=15.0, device=None):
-    w = cpu_inputs(spec, device)
+def cpu_baseline(spec, w, budget_s=15.0):
     heads, batches = oracle_sample_plan(spec)
     est, n, t0 = [], 0, time.perf_counter()
     while n == 0 or (time.perf_counter() - t0 < budget_s and n < 20):
@@ -425,6 +550,85 @@ def cpu_baseline(spec, budget_s=15.0, device=None):
             "sample": (f"{n} oracle step(s) of {spec.name}: sampler rows of {len(batches)} "
                        f"sequence(s) and attention for {heads} of {spec.Hq} query heads, "
                        f"scaled to the full step (B={spec.B}); numpy float64, one thread")}
+
+
+def cpu_baseline_all_cores(spec, w):
+    """The oracle across every host core: one thread per (sequence, KV head)
+    attention task and per sequence's sampler rows, over enough sequences to
+    give every core a task; wall time scaled to the full batch."""
+    import oracle
+    from oracle.sampler import SamplerCfg
+    from tests.util import sub_sequence
+    n = os.cpu_count() or 1
+    G = spec.Hq // spec.Hkv
+    seqs = list(range(min(spec.B, max(1, -(-n // spec.Hkv)))))
+    anc, _, _ = oracle.tree.tree_prepare(w.parent.numpy(), w.ctx_len.numpy())
+    subs = {b: sub_sequence(w, b) for b in seqs}
+    cfg = SamplerCfg(temperature=spec.temperature, top_k=spec.top_k, top_p=spec.top_p,
+                     greedy=spec.greedy)
+
+    def attn_task(b, kvh):
+        q, k, v, table, ctx = subs[b]
+        hs = slice(kvh * G, (kvh + 1) * G)
+        oracle.attention.verify_attention(q[:, :, hs], k[:, :, kvh:kvh + 1], v[:, :, kvh:kvh + 1],
+                                          table, ctx, anc[b:b + 1])
+
+    def samp_task(b):
+        sl = slice(b, b + 1)
+        if spec.is_tree:
+            oracle.sampler.accept_tree_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                             w.draft_tokens[sl].numpy(), w.parent[sl].numpy(),
+                                             w.uniforms[sl].numpy(), cfg)
+        else:
+            oracle.sampler.accept_chain_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                              w.draft_tokens[sl].numpy(),
+                                              w.uniforms[sl].numpy(), cfg)
+
+    tasks = [(attn_task, (b, k)) for b in seqs for k in range(spec.Hkv)] + \
+        [(samp_task, (b,)) for b in seqs]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(lambda t: t[0](*t[1]), tasks))
+    wall = time.perf_counter() - t0
+    step_s = wall * spec.B / len(seqs)
+    return {"value": spec.B * spec.R / step_s, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": (f"{len(seqs)} of {spec.B} sequences of {spec.name} (every row and head), "
+                       f"{len(tasks)} tasks on {n} threads (numpy float64; parts that hold the "
+                       f"interpreter lock serialise), wall time scaled to the full batch")}
+
+
+def parity_sample(spec, step, w, max_seqs=16):
+    """The GPU step's outputs against the oracle on the same inputs: sampler
+    decisions of up to max_seqs sequences (bit-exact except flagged draws) and
+    attention of two sequences (every row, one query head per KV head)."""
+    import oracle
+    from tests.util import cfg_of, np_u64, oracle_attention
+    B = spec.B
+    seqs = list(range(min(B, max_seqs)))
+    sl = slice(0, len(seqs))
+    cfg = cfg_of(spec)
+    if spec.is_tree:
+        ref = oracle.sampler.accept_tree_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                               w.draft_tokens[sl].numpy(), w.parent[sl].numpy(),
+                                               w.uniforms[sl].numpy(), cfg)
+    else:
+        ref = oracle.sampler.accept_chain_batch(w.logits[sl].numpy(), w.draft_probs[sl].numpy(),
+                                                w.draft_tokens[sl].numpy(),
+                                                w.uniforms[sl].numpy(), cfg)
+    g_acc = step.sout["accepted_len"].cpu().numpy()[sl]
+    g_emit = step.sout["emitted"].cpu().numpy()[sl]
+    ok = ~ref["flagged"]
+    mism = int(((g_acc != ref["accepted_len"]) | (g_emit != ref["emitted"]).any(1))[ok].sum())
+    anc = np_u64(step.anc)
+    G = spec.Hq // spec.Hkv
+    heads = [k * G + k % G for k in range(spec.Hkv)]
+    bs = list(range(min(B, 2)))
+    out, _ = oracle_attention(w, anc, batches=bs, heads=heads)
+    g_out = step.attn.out.float().cpu().numpy()
+    err = max(float(np.abs(g_out[b][:, heads] - out[b][:, heads]).max()) for b in bs)
+    return {"sampler_sequences": len(seqs), "flagged": int(ref["flagged"].sum()),
+            "mismatched_unflagged": mism, "attn_sequences": len(bs),
+            "attn_max_abs_err": err, "attn_tolerance": 2e-2}
 
 
 def bench_reference(args, spec):
@@ -456,6 +660,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--per-workload-steps", type=int, default=200)
+    ap.add_argument("--serial", action="store_true",
+                    help="run the sampler after the attention on one stream")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     spec = wl.SPECS[args.workload]
@@ -468,9 +676,16 @@ def main(argv=None):
 
     init_dist(ws, "nccl")
     out = bench_gpu(args, spec, ws, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        dev = torch.device("cuda", local)
+        step = GpuStep(spec, dev, overlap=not args.serial)   # the headline's inputs again
+        step.run()
+        torch.cuda.synchronize()
+        w = step.w.to("cpu")
+        out["parity_sample"] = parity_sample(spec, step, w)
+        out["cpu_baseline"] = cpu_baseline(spec, w)
+        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(spec, w)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(spec, device=torch.device("cuda", local))
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -145,12 +145,15 @@ def test_invisible_nodes_and_stale_cache_do_not_leak():
     assert not np.allclose(out[0, 5], base[0, 5])
 
 
-# ------------------------------------------------------------------ attention, full sizes (sampled)
+# ------------------------------------------------------------------ attention, full sizes
 FULL = ["llama8b_chain", "long_context", "batched_serving_a75", "draft_tree"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_outputs(name):
+def test_full_size_outputs(name):
+    """The bench's launch at full size: every sequence and every block row, for one
+    query head of every KV head (a different one per sequence) plus the first and
+    last query heads, compared element by element with the oracle."""
     spec = wl.SPECS[name]
     w = wl.make_attention_inputs(spec, device=DEV)
     g = w
@@ -159,17 +162,17 @@ def test_full_size_sampled_outputs(name):
                               num_splits=spec.num_splits)
     torch.cuda.synchronize()
     out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
     anc_np = np_u64(anc)
-    rng = np.random.default_rng(0)
     B, R, Hq, _ = w.q.shape
-    bs = sorted(set(rng.integers(0, B, size=min(B, 3)).tolist()))
-    rows = sorted(set([0, R - 1] + rng.integers(0, R, size=2).tolist()))
-    heads = sorted(set([0, Hq - 1] + rng.integers(0, Hq, size=2).tolist()))
-    ref, lref = oracle_attention(w, anc_np, batches=bs, rows=rows, heads=heads)
-    for b in bs:
-        for i in rows:
-            for h in heads:
-                err = np.abs(out[b, i, h] - ref[b, i, h]).max()
-                assert err < BF16_ATOL, (b, i, h, err)
-                assert abs(float(lse[b, i, h]) - lref[b, i, h]) < 1e-3
+    G = Hq // spec.Hkv
     assert np.isfinite(out).all()
+    worst = 0.0
+    for b in range(B):
+        heads = sorted({0, Hq - 1} | {k * G + (b + k) % G for k in range(spec.Hkv)})
+        ref, lref = oracle_attention(w, anc_np, batches=[b], heads=heads)
+        err = np.abs(out[b][:, heads] - ref[b][:, heads]).max()
+        worst = max(worst, float(err))
+        assert err < BF16_ATOL, (b, err)
+        assert np.abs(lse[b][:, heads] - lref[b][:, heads]).max() < 1e-3, b
+    print(f"{name}: {B} sequences x {R} rows, max abs error {worst:.2e}")

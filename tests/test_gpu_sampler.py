@@ -7,6 +7,7 @@ within 1e-6 relative.  Statistical tests check the lossless property and the
 closed form of the expected tokens per step on the GPU kernel itself.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -18,7 +19,7 @@ import speculative_decoding_verification_76_gb300 as sv
 from oracle.sampler import SamplerCfg
 from speculative_decoding_verification_76_gb300 import workloads as wl
 from tests.conftest import load_golden
-from tests.util import P_RTOL, cfg_of
+from tests.util import FLAG_CAP, P_RTOL, cfg_of, record_flags
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -45,16 +46,25 @@ def run_tree(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=True):
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare(gpu, ref, tree=False, max_flag_frac=0.5):
+def compare(gpu, ref, tree=False, max_flagged=None):
+    """Bit-exact accepted_len / emitted (and path) on every unflagged sequence.
+
+    The flagged count is recorded for the end-of-run report and capped: at most
+    FLAG_CAP of the sequences (at least one) unless a test constructs
+    near-threshold rows on purpose and passes its own cap."""
+    B = len(ref["flagged"])
+    n_flag = int(ref["flagged"].sum())
+    record_flags(os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], n_flag, B)
+    cap = max(1, int(FLAG_CAP * B)) if max_flagged is None else max_flagged
+    assert n_flag <= cap, f"{n_flag} of {B} sequences flagged (cap {cap})"
     ok = ~ref["flagged"]
-    assert ok.mean() >= 1 - max_flag_frac, f"too many flagged: {ref['flagged'].sum()}"
     np.testing.assert_array_equal(gpu["accepted_len"][ok], ref["accepted_len"][ok])
     np.testing.assert_array_equal(gpu["emitted"][ok], ref["emitted"][ok])
     if tree:
         np.testing.assert_array_equal(gpu["path"][ok], ref["path"][ok])
     # flagged sequences: still a valid outcome (accepted prefix of the drafts)
     assert (gpu["accepted_len"] >= 0).all()
-    return int(ref["flagged"].sum())
+    return n_flag
 
 
 def check_p(gpu_p, ref, logits=None, cfg=None):
@@ -247,7 +257,7 @@ def test_full_vocab_chain(name):
 
 
 def test_batched_serving_topp_sample():
-    # B=8 (40 rows x 8-CTA clusters: the many-row path) and B=2 (the cluster path)
+    # B=8 (40 rows: the many-row path) and B=2 (the cluster path)
     for name in ("batched_serving_a45", "batched_serving_a75"):
         for B in (8, 2):
             spec = wl.SPECS[name].with_(B=B)
@@ -257,6 +267,20 @@ def test_batched_serving_topp_sample():
             gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
                              want_p=False)
             compare(gpu2, ref)
+
+
+@pytest.mark.parametrize("name", ["batched_serving_a45", "batched_serving_a75"])
+def test_batched_serving_full_size(name):
+    """The bench's sampler launch at full size: B = 64 sequences, 320 rows of
+    152,064 logits (several rounds of the one-CTA-per-row kernel), the bench's
+    seed, with and without p returned."""
+    spec = wl.SPECS[name]
+    w, gpu, ref = chain_case(spec, spec.seed)
+    compare(gpu, ref)
+    check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
+    gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
+                     want_p=False)
+    compare(gpu2, ref)
 
 
 STREAM_SHAPES = [
@@ -290,7 +314,9 @@ def test_many_rows_floor_fallbacks(name, kw, sd, clustered, V):
                                             want_p=True)
     for want_p in (True, False):
         gpu = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg, want_p)
-        compare(gpu, ref, max_flag_frac=1.0 if name == "flat_topp" else 0.5)
+        # flat_topp: every token is lighter than the flag margin, so the top-p cutoff is
+        # ambiguous by construction and may flag every sequence
+        compare(gpu, ref, max_flagged=spec.B if name == "flat_topp" else None)
         if want_p:
             check_p(gpu["p"], ref, w.logits.numpy(), cfg)
 
