@@ -386,3 +386,54 @@ def accept_tree_batch(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=Fals
         out["p"] = np.stack([r["p"] for r in res])
         out["alt_sizes"] = [r["alt_sizes"] for r in res]
     return out
+
+
+# ---------------------------------------------------------------- served logits: bans, penalties
+def row_prefix_tokens(block_tokens, parent, i: int):
+    """Block tokens already in front of block row i (the row scores after them).
+
+    Chain (parent None): block_tokens [R-1] are the drafts; row i follows drafts
+    0 .. i-1.  Tree: block_tokens [R] are the node tokens (node 0, the anchor,
+    is not listed -- the anchor belongs to the history); row v follows the
+    tokens of its ancestors below the anchor and its own."""
+    if parent is None:
+        return [int(t) for t in block_tokens[:i]]
+    out, v = [], int(i)
+    while v > 0:
+        out.append(int(block_tokens[v]))
+        v = int(parent[v])
+    return out[::-1]
+
+
+def served_logits(logits_row, seen, penalty: float = 1.0, banned=()):
+    """One target row as served ("Speculative Decoding" (atlas), "Greedy,
+    sampling and the real sampler": p must include token bans and repetition
+    penalties).  [READING: the pages give no formula]  The common multiplicative
+    repetition penalty: every distinct token id in `seen` (the history and the
+    row's block prefix) has its logit l replaced by l / penalty if l > 0, else
+    l * penalty -- once, however often it occurs; then every banned id gets -inf.
+    Ids outside [0, V) are ignored.  Computed in fp32, the arithmetic of the
+    served logits."""
+    out = np.array(logits_row, dtype=np.float32, copy=True)
+    V = out.shape[0]
+    th = np.float32(penalty)
+    for t in sorted({int(t) for t in seen if 0 <= int(t) < V}):
+        out[t] = out[t] / th if out[t] > 0 else out[t] * th
+    for t in banned:
+        if 0 <= int(t) < V:
+            out[int(t)] = -np.inf
+    return out
+
+
+def served_logits_batch(logits, history, block_tokens, parent, penalty, banned):
+    """logits [B,R,V]; history [B,H] (-1 unused); block_tokens chain [B,R-1] or
+    tree [B,R]; parent [B,R] or None (chain)."""
+    logits = np.asarray(logits, dtype=np.float32)
+    out = np.empty_like(logits)
+    B, R, _ = logits.shape
+    for b in range(B):
+        hist = [int(t) for t in np.asarray(history[b]) if int(t) >= 0]
+        for i in range(R):
+            pre = row_prefix_tokens(block_tokens[b], None if parent is None else parent[b], i)
+            out[b, i] = served_logits(logits[b, i], hist + pre, penalty, banned)
+    return out

@@ -460,3 +460,43 @@ def test_tree_topp_ambiguity_flags_only_when_outcome_changes():
     # the same rows without ambiguity (top_p clear of the boundary) are not flagged
     clear = osm.accept_tree(logits, q, [-1, 2], parent, [0.5, 0.1], SamplerCfg(top_p=0.85))
     assert not clear["flagged"] and clear["path"] == [1]
+
+
+# ---------------------------------------------------------------- served logits (bans, penalties)
+def test_served_logits_closed_forms():
+    l = np.array([2.0, -1.5, 0.0, 3.0, -4.0], dtype=np.float32)
+    out = osm.served_logits(l, [0, 1, 2, 0, 0, -1, 99], penalty=2.0)
+    # positive logits are divided, non-positive ones multiplied, once per distinct id;
+    # ids outside the vocabulary are ignored
+    np.testing.assert_array_equal(out, np.array([1.0, -3.0, 0.0, 3.0, -4.0], np.float32))
+    assert out.dtype == np.float32
+    # penalty 1 and no bans: the identity
+    np.testing.assert_array_equal(osm.served_logits(l, [0, 1, 3], 1.0), l)
+    # bans: -inf whatever the penalty did, and p = 0 there
+    out = osm.served_logits(l, [3], penalty=1.3, banned=[3, 4, 7])
+    assert out[3] == -np.inf and out[4] == -np.inf and out[0] == l[0]
+    p, _ = osm.target_distribution(out, SamplerCfg())
+    assert p[3] == 0.0 and p[4] == 0.0 and p.sum() == pytest.approx(1.0)
+
+
+def test_served_logits_penalty_lowers_seen_tokens():
+    rng = np.random.default_rng(8)
+    l = rng.normal(0, 3, 300).astype(np.float32)
+    seen = rng.integers(0, 300, 40)
+    p0, _ = osm.target_distribution(l, SamplerCfg())
+    p1, _ = osm.target_distribution(osm.served_logits(l, seen, penalty=1.5), SamplerCfg())
+    s = np.unique(seen)
+    rest = np.setdiff1d(np.arange(300), s)
+    # every seen token loses probability relative to every unseen one
+    assert np.all(p1[s] / p0[s] < p1[rest[0]] / p0[rest[0]])
+    np.testing.assert_allclose(p1[rest] / p0[rest], p1[rest[0]] / p0[rest[0]], rtol=1e-9)
+
+
+def test_row_prefix_tokens_chain_and_fox_tree():
+    drafts = [11, 12, 13]
+    assert [osm.row_prefix_tokens(drafts, None, i) for i in range(4)] == \
+        [[], [11], [11, 12], [11, 12, 13]]
+    toks = [-1, 10, 20, 21, 11, 30]      # fox, jumps, over, high, runs, away
+    pre = [osm.row_prefix_tokens(toks, FOX_PARENT, v) for v in range(6)]
+    # "over" scores after fox jumps over; "away" after fox runs away; siblings never mix
+    assert pre == [[], [10], [10, 20], [10, 21], [11], [11, 30]]
