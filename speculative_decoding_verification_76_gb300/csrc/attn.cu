@@ -12,47 +12,37 @@
 // unnormalised softmax partial with its log-sum-exp, and a combine rescales
 // the partials by exp(lse_s - max lse).
 //
-// GB300 design.  One CTA per (chunk, KV head x row tile, sequence).  All
-// R*G query rows of a KV head (G = Hq/Hkv) share each K/V tile, so the KV
-// stream -- the bytes that bound this step -- is read once.  A producer warp
-// streams 64-token K/V stages with TMA (128-byte swizzle, one 16-token box
-// per page segment) through a 4-deep mbarrier ring; eight consumer warps run
-// QK^T and PV on the tensor cores (bf16 in, fp32 accumulate) with the
-// online softmax in registers.  Warps are (row group of 16) x (token group);
-// token groups take alternate stages and merge through shared memory at
-// the end.  An fp32 CUDA-core kernel serves fp32 caches.
+// GB300 design.  Two partial passes share the split plan and the partial
+// layout [B, Hkv, RGpad, S, D] (+ log2-domain LSE):
+//  * up to 64 query rows per KV head (the chain shapes: R * G = 20 .. 64):
+//    attn_partial_bf16 below.  One CTA per (chunk, KV head x row tile,
+//    sequence); all R*G rows of a KV head share each K/V tile, so the KV
+//    stream -- the bytes that bound these shapes -- is read once.  Four copy
+//    warps stream K/V stages with 16-byte cp.async (64 contiguous bytes per
+//    thread, one page lookup per token, 128-byte swizzle) into a 3-stage
+//    (128-token) or 6-stage (64-token) mbarrier ring; eight MMA warps run
+//    QK^T and PV with mma.sync m16n8k16 (bf16 in, fp32 accumulate) and the
+//    online softmax in registers.  Warps are (row group of 16) x (token group)
+//    and the token groups merge through shared memory at the end.
+//  * more than 64 rows per KV head (draft trees, long chains): the tcgen05
+//    pass in attn_tc.cu (128-row MMAs, tensor-memory accumulators).
+// An fp32 CUDA-core kernel serves fp32 caches.
 #include <algorithm>
 
-#include "common.cuh"
+#include "attn.cuh"
 
 namespace {
 
-constexpr int kStageTokens = 64;       // granularity of chunks (and the fp32 path)
+using attn::AttnParams;
+using attn::kLog2e;
+using attn::kMaxChunk;
+using attn::kStageTokens;
+
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kQStride = 136;  // bf16 per Q row in shared memory (272 B: conflict-free ldmatrix)
-constexpr int kMaxChunk = 4096;
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct AttnParams {
-  const __nv_bfloat16* q;  // [B,R,Hq,D]
-  const float* qf;         // fp32 path
-  const float* kf;
-  const float* vf;
-  const void* k;  // bf16 caches
-  const void* v;
-  const int32_t* block_table;
-  const int32_t* ctx_len;
-  const uint64_t* anc_mask;
-  float* o_part;    // [B,Hkv,RGpad,S,D]
-  float* lse_part;  // [B,Hkv,RGpad,S]   (log2 domain)
-  int32_t* err;
-  int B, R, Hq, Hkv, G, D, page_size, max_pages, num_pages;
-  int RG, RGpad, row_tiles, chunk, S;
-  float scale_log2;
-};
 
 // ------------------------------------------------------------------ bf16 tensor-core kernel
 // Stages in the K/V ring: as many as fit beside the Q tile (<= 227 KB).
@@ -65,7 +55,7 @@ __host__ __device__ constexpr int stage_tokens() {
 // Stages in the ring: as many as fit beside the Q tile (<= 227 KB).
 template <int NRG>
 __host__ __device__ constexpr int stages_for() {
-  return NRG == 2 ? 3 : (NRG >= 8 ? 5 : 6);
+  return NRG == 2 ? 3 : 6;
 }
 
 template <int NRG>
@@ -580,10 +570,15 @@ int num_sms() {
 
 struct Plan {
   int G, RG, NRG, RT, row_tiles, RGpad, chunk, S;
-  bool tc;  // tensor-core path
+  bool tc;   // warp-MMA tensor-core path (bf16, at most 64 rows per KV head)
+  int NM;    // > 0: the tcgen05 path with NM 128-row tiles per CTA (bf16, > 64 rows)
 };
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Rows per KV head above which the partial pass runs on tcgen05 (tensor-memory
+// accumulators, 128-row MMAs): the draft-tree and long-chain shapes.
+constexpr int kTcgen05MinRows = 65;
 
 bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_pages, int num_splits,
                bool bf16, Plan* pl) {
@@ -592,8 +587,15 @@ bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_page
   pl->tc = bf16;
   pl->G = Hq / Hkv;
   pl->RG = R * pl->G;
-  if (bf16) {
-    pl->NRG = pl->RG <= 32 ? 2 : pl->RG <= 64 ? 4 : 8;
+  pl->NM = 0;
+  if (bf16 && pl->RG >= kTcgen05MinRows) {
+    pl->NM = pl->RG > 128 ? 2 : 1;
+    pl->NRG = 0;
+    pl->RT = 128 * pl->NM;
+    pl->row_tiles = (pl->RG + pl->RT - 1) / pl->RT;
+    pl->RGpad = pl->row_tiles * pl->RT;
+  } else if (bf16) {
+    pl->NRG = pl->RG <= 32 ? 2 : 4;
     pl->RT = 16 * pl->NRG;
     pl->row_tiles = (pl->RG + pl->RT - 1) / pl->RT;
     pl->RGpad = pl->row_tiles * pl->RT;
@@ -742,12 +744,10 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
 
   if (phase & kPartials) {
     spec_status rc;
-    if (bf16) {
-      switch (pl.NRG) {
-        case 2: rc = launch_bf16<2>(prm, pl, st); break;
-        case 4: rc = launch_bf16<4>(prm, pl, st); break;
-        default: rc = launch_bf16<8>(prm, pl, st); break;
-      }
+    if (bf16 && pl.NM > 0) {
+      rc = attn::launch_partial_tc(prm, pl.NM, st);
+    } else if (bf16) {
+      rc = pl.NRG == 2 ? launch_bf16<2>(prm, pl, st) : launch_bf16<4>(prm, pl, st);
     } else {
       dim3 grid(pl.S, Hkv, B);
       attn_partial_f32<<<grid, 128, 0, st>>>(prm);
