@@ -28,8 +28,10 @@ struct AttnParams {
   float scale_log2;
 };
 
-// The tcgen05 partial pass: 128 * NM query rows of one KV head per CTA (NM = 1
-// or 2), grid (Hkv * row_tiles, S, B).  Defined in attn_tc.cu.
-spec_status launch_partial_tc(const AttnParams& prm, int NM, cudaStream_t st);
+// The tcgen05 partial pass: 128 query rows of one KV head per CTA, 128-token
+// stages, grid (Hkv * row_tiles, S, B).  Defined in attn_tc.cu.
+constexpr int kTcRows = 128;
+constexpr int kTcStageTokens = 128;
+spec_status launch_partial_tc(const AttnParams& prm, cudaStream_t st);
 
 }  // namespace attn
