@@ -571,7 +571,7 @@ int num_sms() {
 struct Plan {
   int G, RG, NRG, RT, row_tiles, RGpad, chunk, S;
   bool tc;   // warp-MMA tensor-core path (bf16, at most 64 rows per KV head)
-  int NM;    // 1: the tcgen05 path, 128-row tiles (bf16, more than 64 rows)
+  int NM;    // > 0: the tcgen05 path with NM 128-row tiles per CTA (bf16, > 64 rows)
 };
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -589,9 +589,10 @@ bool make_plan(int B, int R, int Hq, int Hkv, int D, int page_size, int max_page
   pl->RG = R * pl->G;
   pl->NM = 0;
   if (bf16 && pl->RG >= kTcgen05MinRows) {
-    pl->NM = 1;
+    // two 128-row tiles per CTA (sharing each K/V stage) beyond 128 rows
+    pl->NM = pl->RG > attn::kTcRows ? 2 : 1;
     pl->NRG = 0;
-    pl->RT = attn::kTcRows;
+    pl->RT = attn::kTcRows * pl->NM;
     pl->row_tiles = (pl->RG + pl->RT - 1) / pl->RT;
     pl->RGpad = pl->row_tiles * pl->RT;
   } else if (bf16) {
@@ -746,7 +747,7 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   if (phase & kPartials) {
     spec_status rc;
     if (bf16 && pl.NM > 0) {
-      rc = attn::launch_partial_tc(prm, st);
+      rc = attn::launch_partial_tc(prm, pl.RT, st);
     } else if (bf16) {
       rc = pl.NRG == 2 ? launch_bf16<2>(prm, pl, st) : launch_bf16<4>(prm, pl, st);
     } else {

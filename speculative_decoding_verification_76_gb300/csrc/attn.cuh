@@ -28,10 +28,11 @@ struct AttnParams {
   float scale_log2;
 };
 
-// The tcgen05 partial pass: 128 query rows of one KV head per CTA, 128-token
-// stages, grid (Hkv * row_tiles, S, B).  Defined in attn_tc.cu.
+// The tcgen05 partial pass: rows_per_cta (128 or 256) query rows of one KV head
+// per CTA, 128-token stages, grid (Hkv * row_tiles, S, B).  Defined in
+// attn_tc.cu.
 constexpr int kTcRows = 128;
 constexpr int kTcStageTokens = 128;
-spec_status launch_partial_tc(const AttnParams& prm, cudaStream_t st);
+spec_status launch_partial_tc(const AttnParams& prm, int rows_per_cta, cudaStream_t st);
 
 }  // namespace attn
