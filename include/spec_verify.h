@@ -329,6 +329,67 @@ spec_status spec_kv_commit(void* k_cache, void* v_cache, int elem_bytes, int num
                            int32_t* new_len,
                            int32_t* keep_pages, int32_t* status_per_seq, void* stream);
 
+/* ------------------------------------------------------------------------
+ * spec_append_block -- write the proposed block into the paged cache, keys
+ * rotated for their position.  "Speculative Decoding" (atlas), "Chains, trees
+ * and visibility": position ids follow depth rather than flattened storage
+ * order, so tree node j is stored at slot ctx_len + j but rotated for its
+ * position id ctx_len + depth(j) (spec_tree_prepare's pos_ids).  Run it before
+ * spec_verify_attn, which reads block row j at position ctx_len + j.
+ *
+ *   k_new, v_new [B,R,Hkv,D] dtype: the block's keys before rotation and its
+ *            values.
+ *   q        [B,R,Hq,D] dtype (nullable): the block's queries, rotated in
+ *            place at the same positions (what spec_verify_attn then reads).
+ *   k_cache, v_cache [num_pages,page_size,Hkv,D] dtype: row j of sequence b is
+ *            written at position ctx_len[b] + j of its page list (the key
+ *            rotated, the value as given).
+ *   pos_ids  [B,R] int32 (NULL: a chain, ctx_len[b] + j).
+ *   rope_base > 1: pair (x_i, x_{i+D/2}) at position t is rotated by the
+ *            angle t * rope_base^(-2i/D) (the split-half rotary form; the pages
+ *            do not print the rotation).  Angles are formed in double precision
+ *            and reduced before the fp32 sine / cosine; rows rotate in fp32 and
+ *            are rounded to the cache dtype.
+ *   status_per_seq [B] int32 out (nullable): SPEC_SEQ_BAD_TREE if a row's page
+ *            is missing or out of range, ctx_len < 0, the block would run past
+ *            the block table, or a position id is negative; such a sequence is
+ *            left untouched (no row written, no query rotated).
+ *   D in {64,128}, 1 <= R <= 64.  Device pointers, async on the stream.
+ * ---------------------------------------------------------------------- */
+spec_status spec_append_block(const void* k_new, const void* v_new, void* q, spec_dtype dtype,
+                              void* k_cache, void* v_cache, int num_pages, int page_size,
+                              const int32_t* block_table, int max_pages, const int32_t* ctx_len,
+                              const int32_t* pos_ids, int B, int R, int Hq, int Hkv, int D,
+                              float rope_base, int32_t* status_per_seq, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_logits_penalize -- the target logits as served, in place, before
+ * spec_accept_sample(_tree).  "Speculative Decoding" (atlas), "Greedy,
+ * sampling and the real sampler": p must include the transformations of the
+ * served sampler -- temperature, truncation, token bans and repetition
+ * penalties (the first two are spec_sampler's; this call applies the others).
+ * The pages give no penalty formula; the one applied is the common
+ * multiplicative form: every distinct token id in a row's prefix has its logit
+ * l replaced by l / penalty if l > 0, else l * penalty (once, however often it
+ * occurs), in fp32; then every banned id gets -inf.  A row's prefix is the
+ * sequence's history plus the block tokens in front of the row: a chain's
+ * drafts 0 .. i-1 for row i, a tree node's ancestors below the anchor and the
+ * node itself.  The draft distribution q is the drafter's and is not touched.
+ *
+ *   logits   [B,R,V] fp32, updated in place.
+ *   history  [B,H] int32: tokens already in each sequence (including the
+ *            pending anchor); ids outside [0, V) (e.g. -1 padding) are skipped.
+ *   block_tokens chain: [B,R-1] drafts; tree: [B,R] node tokens (node 0
+ *            unused).  parent [B,R] int32 for a tree, NULL for a chain.
+ *   penalty  > 0 (1: none).  banned [n_banned] int32 ids, shared by every
+ *            sequence (nullable when n_banned == 0).
+ *   1 <= R <= 64, V <= 172032.
+ * ---------------------------------------------------------------------- */
+spec_status spec_logits_penalize(float* logits, int B, int R, int V, const int32_t* history,
+                                 int H, const int32_t* block_tokens, const int32_t* parent,
+                                 float penalty, const int32_t* banned, int n_banned,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

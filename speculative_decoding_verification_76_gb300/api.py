@@ -28,6 +28,7 @@ EXPORTS = (
     "spec_verify_attn_combine", "spec_accept_sample_workspace_size",
     "spec_accept_sample", "spec_accept_sample_tree", "spec_workspace_error",
     "spec_kv_commit", "spec_verify_attn_noalloc", "spec_verify_attn_noalloc_error",
+    "spec_append_block", "spec_logits_penalize",
 )
 
 
@@ -105,6 +106,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_attn_noalloc.restype = _I
     lib.spec_verify_attn_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _I, _I, _I,
                                              _I, _I, ctypes.c_float, _I, _P, _P, _P]
+    lib.spec_append_block.restype = _I
+    lib.spec_append_block.argtypes = [_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I,
+                                      _I, _I, ctypes.c_float, _P, _P]
+    lib.spec_logits_penalize.restype = _I
+    lib.spec_logits_penalize.argtypes = [_P, _I, _I, _I, _P, _I, _P, _P, ctypes.c_float, _P, _I,
+                                         _P]
     lib.spec_verify_attn_noalloc_error.restype = _I
     lib.spec_verify_attn_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
     _lib = lib
@@ -204,6 +211,69 @@ def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.T
                               _ptr(accepted_len), _ptr(path), _ptr(parent), B, R, _ptr(new_len),
                               _ptr(keep_pages), _ptr(status), _stream(stream)))
     return new_len, keep_pages, status
+
+
+def append_block(k_new, v_new, k_cache, v_cache, block_table, ctx_len, pos_ids=None, q=None,
+                 rope_base: float = 10000.0, status=None, stream=None):
+    """Write the block's K/V rows (keys rotated at pos_ids; NULL: chain positions)
+    into the paged cache at ctx + j, and rotate q [B,R,Hq,D] in place if given.
+    Returns status [B]."""
+    lib = load()
+    dt = k_new.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("k_new must be bf16 or fp32")
+    B, R, Hkv, D = k_new.shape
+    npg, P = k_cache.shape[0], k_cache.shape[1]
+    _need(k_new, "k_new", dt)
+    _need(v_new, "v_new", dt, k_new.shape)
+    _need(k_cache, "k_cache", dt)
+    _need(v_cache, "v_cache", dt, k_cache.shape)
+    if tuple(k_cache.shape[2:]) != (Hkv, D):
+        raise ValueError("cache heads / head_dim differ from the block's")
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx_len, "ctx_len", torch.int32, (B,))
+    if pos_ids is not None:
+        _need(pos_ids, "pos_ids", torch.int32, (B, R))
+    Hq = 0
+    if q is not None:
+        _need(q, "q", dt)
+        if q.shape[0] != B or q.shape[1] != R or q.shape[3] != D:
+            raise ValueError("q must be [B, R, Hq, D]")
+        Hq = q.shape[2]
+    status = torch.empty((B,), dtype=torch.int32, device=k_new.device) if status is None \
+        else status
+    _check("spec_append_block",
+           lib.spec_append_block(_ptr(k_new), _ptr(v_new), _ptr(q),
+                                 SPEC_BF16 if dt == torch.bfloat16 else SPEC_F32, _ptr(k_cache),
+                                 _ptr(v_cache), npg, P, _ptr(block_table), block_table.shape[1],
+                                 _ptr(ctx_len), _ptr(pos_ids), B, R, Hq, Hkv, D,
+                                 float(rope_base), _ptr(status), _stream(stream)))
+    return status
+
+
+def logits_penalize(logits, history=None, block_tokens=None, parent=None, penalty: float = 1.0,
+                    banned=None, stream=None):
+    """Repetition penalty over each row's prefix, then bans, on logits [B,R,V] in place."""
+    lib = load()
+    _need(logits, "logits", torch.float32)
+    B, R, V = logits.shape
+    H = 0
+    if history is not None:
+        _need(history, "history", torch.int32)
+        H = history.shape[1]
+    if block_tokens is not None:
+        _need(block_tokens, "block_tokens", torch.int32)
+    if parent is not None:
+        _need(parent, "parent", torch.int32, (B, R))
+    nb = 0
+    if banned is not None:
+        _need(banned, "banned", torch.int32)
+        nb = banned.numel()
+    _check("spec_logits_penalize",
+           lib.spec_logits_penalize(_ptr(logits), B, R, V, _ptr(history), H, _ptr(block_tokens),
+                                    _ptr(parent), float(penalty), _ptr(banned), nb,
+                                    _stream(stream)))
+    return logits
 
 
 # ------------------------------------------------------------------ attention
