@@ -45,8 +45,6 @@ UNIT = "positions/s"
 DEFAULT_WORKLOAD = "batched_serving_a75"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
-# the attention kernel sources an ncu traffic record must have been taken on
-TRAFFIC_SOURCES = ("attn.cu", "attn_tc.cu", "common.cuh", "tc_ptx.cuh")
 
 
 # ------------------------------------------------------------------ helpers
@@ -107,9 +105,10 @@ def bf16_peak():
         return 1900.0, "fallback 1.9 PFLOP/s"
 
 
-def source_hash() -> str:
+def source_hash(files) -> str:
+    """Hash of the named kernel sources (a traffic record holds for them only)."""
     h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
+    for f in files:
         p = os.path.join(ROOT, "speculative_decoding_verification_76_gb300", "csrc", f)
         if os.path.exists(p):
             with open(p, "rb") as fh:
@@ -118,14 +117,14 @@ def source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the partial kernel from an ncu capture, if
-    the capture was taken on the current kernel source."""
+    """DRAM bytes per launch of the partial kernel from an ncu capture, if the
+    capture was taken on the current source of the kernel it names."""
     path = os.path.join(ROOT, "profiles", "attn_partial_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_sha") == source_hash():
+        if e and e.get("source_sha") == source_hash(e.get("sources", [])):
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -404,7 +403,7 @@ def bench_gpu(args, spec, ws, rank, local):
         "step_hbm_frac_all_q_rows": rec["step_hbm_frac_all_q_rows"],
         "step_algorithmic_bytes_all_q_rows": nbytes["step_all_q"],
         "attn_num_splits": rec["attn_num_splits"], "sampler_us": rec["sampler_us"],
-        "roofline": {"bound": "hbm", "kernel": "attention partial pass (split-K)",
+        "roofline": {"bound": "hbm", "kernel": partial_kernel_name(spec),
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": nbytes["attn"], "mean_launch_us": part_mean * 1e6,
@@ -421,6 +420,18 @@ def bench_gpu(args, spec, ws, rank, local):
     return out
 
 
+def partial_kernel_name(spec) -> str:
+    """The partial-pass kernel the library's plan runs for this shape."""
+    rows = spec.R * spec.Hq // spec.Hkv
+    if spec.kv_dtype == "f32":
+        return "attn_partial_f32 (CUDA cores)"
+    if rows > 128:
+        return "attn_partial_tc2 (tcgen05, two 128-row tiles per CTA)"
+    if rows > 64:
+        return "attn_partial_tc1 (tcgen05, one 128-row tile per CTA)"
+    return "attn_partial_bf16 (warp-level mma.sync)"
+
+
 def per_workload(args, headline, ws, dev, flush_l2, peak):
     """The other configurations (the tiny one is a parity case only), each in its
     own graph, timed like the headline."""
@@ -433,6 +444,7 @@ def per_workload(args, headline, ws, dev, flush_l2, peak):
         nbytes = wl.algorithmic_bytes(spec, ctx)
         t = time_step(step, args.per_workload_steps, args.warmup, flush_l2, ws)
         rec = step_record(spec, step, t, nbytes, peak, ws, dev)
+        rec["attn_partial_kernel"] = partial_kernel_name(spec)
         rec.update(acceptance_stats(spec, step.sout["accepted_len"].cpu().numpy()))
         res[name] = rec
         del step
