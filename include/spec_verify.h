@@ -159,6 +159,26 @@ spec_status spec_verify_attn_combine(const void* q, const void* k_cache, const v
                                      void* out, float* lse_out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_debug_attn_fault -- TEST ONLY: make the bounded device waits of the
+ * attention partial passes run out on purpose.  The pages have no
+ * counterpart; this exists so that a test can show that a wait that runs out
+ * ends the kernel with an error word instead of hanging the GPU.
+ *
+ *   withhold_stage  >= 0: in every partial-pass CTA launched from now on, the
+ *                   copy warps never signal that K/V stage withhold_stage has
+ *                   landed, so the waits on it (and those behind it) run out;
+ *                   -1: normal operation.
+ *   wait_limit_ns   bound of every wait of the partial passes; 0 restores the
+ *                   default (2 s).
+ * The setting is process-wide and applies to every later call on every
+ * device; restore it with (-1, 0).  A CTA whose wait ran out sets
+ * SPEC_ERR_MBAR_TIMEOUT in the workspace error word (spec_workspace_error),
+ * lets its own copies and tensor-core operations finish, frees its tensor
+ * memory and returns; the call's outputs are then unspecified.
+ * ---------------------------------------------------------------------- */
+spec_status spec_debug_attn_fault(int withhold_stage, unsigned long long wait_limit_ns);
+
+/* ------------------------------------------------------------------------
  * spec_verify_attn_noalloc -- spec_verify_attn for callers that cannot
  * allocate device memory.  (The pages have no counterpart: this is a
  * deployment convenience, not part of the method.)

@@ -28,7 +28,7 @@ EXPORTS = (
     "spec_verify_attn_combine", "spec_accept_sample_workspace_size",
     "spec_accept_sample", "spec_accept_sample_tree", "spec_workspace_error",
     "spec_kv_commit", "spec_verify_attn_noalloc", "spec_verify_attn_noalloc_error",
-    "spec_append_block", "spec_logits_penalize",
+    "spec_append_block", "spec_logits_penalize", "spec_debug_attn_fault",
 )
 
 
@@ -112,6 +112,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_logits_penalize.restype = _I
     lib.spec_logits_penalize.argtypes = [_P, _I, _I, _I, _P, _I, _P, _P, ctypes.c_float, _P, _I,
                                          _P]
+    lib.spec_debug_attn_fault.restype = _I
+    lib.spec_debug_attn_fault.argtypes = [_I, ctypes.c_ulonglong]
     lib.spec_verify_attn_noalloc_error.restype = _I
     lib.spec_verify_attn_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
     _lib = lib

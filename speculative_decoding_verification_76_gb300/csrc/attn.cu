@@ -28,6 +28,7 @@
 //    pass in attn_tc.cu (128-row MMAs, tensor-memory accumulators).
 // An fp32 CUDA-core kernel serves fp32 caches.
 #include <algorithm>
+#include <atomic>
 
 #include "attn.cuh"
 
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
     const int pshift = __ffs(P) - 1;
     for (int k = 0; k < nst; ++k) {
       const int slot = k % kNumStages;
-      if (k >= kNumStages && !mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err)) break;
+      if (k >= kNumStages && !mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err, p.wait_ns)) break;
       const uint32_t sbase = smem_u32(stages + slot * kStageBytes);
 #pragma unroll
       for (int j = 0; j < ST / 32; ++j) {
@@ -169,9 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
                        : "memory");
         }
       }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
-                       smem_u32(&full[slot]))
-                   : "memory");
+      if (k != p.withhold_stage)  // (a test can withhold one stage: its waiters time out)
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         smem_u32(&full[slot]))
+                     : "memory");
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
 
   for (int k = 0; k < nst; ++k) {
     const int slot = k % kNumStages;
-    if (!mbar_wait(&full[slot], (k / kNumStages) & 1, p.err)) break;
+    if (!mbar_wait(&full[slot], (k / kNumStages) & 1, p.err, p.wait_ns)) break;
     const uint32_t st = smem_u32(stages + slot * kStageBytes);
     const int tb = c0 + k * ST + tsb;   // first cache position of the sub-block
 
@@ -683,6 +685,11 @@ namespace {
 
 enum Phase { kPartials = 1, kCombine = 2, kBoth = 3 };
 
+// Test-only fault setting of the partial passes (spec_debug_attn_fault): a
+// stage whose arrival the copy warps withhold, and the bound of every wait.
+std::atomic<int> g_withhold_stage{-1};
+std::atomic<unsigned long long> g_wait_ns{SPEC_WAIT_NS};
+
 spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_cache,
                              spec_dtype dtype, int page_size, int num_pages,
                              const int32_t* block_table, int max_pages, const int32_t* ctx_len,
@@ -742,6 +749,8 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   prm.S = pl.S;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   prm.scale_log2 = sc * kLog2e;
+  prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  prm.withhold_stage = g_withhold_stage.load(std::memory_order_relaxed);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (phase & kPartials) {
@@ -774,6 +783,13 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
 #define SPEC_ATTN_FWD                                                                        \
   q, k_cache, v_cache, dtype, page_size, num_pages, block_table, max_pages, ctx_len, anc_mask, \
       B, R, Hq, Hkv, D, scale, num_splits, workspace, workspace_bytes
+
+extern "C" spec_status spec_debug_attn_fault(int withhold_stage, unsigned long long wait_limit_ns) {
+  if (withhold_stage < -1) return SPEC_EINVAL;
+  g_withhold_stage.store(withhold_stage);
+  g_wait_ns.store(wait_limit_ns ? wait_limit_ns : SPEC_WAIT_NS);
+  return SPEC_OK;
+}
 
 extern "C" spec_status spec_verify_attn(SPEC_ATTN_ARGS, void* out, float* lse_out, void* stream) {
   return verify_attn_impl(SPEC_ATTN_FWD, out, lse_out, stream, kBoth);

@@ -26,6 +26,8 @@ struct AttnParams {
   int B, R, Hq, Hkv, G, D, page_size, max_pages, num_pages;
   int RG, RGpad, row_tiles, chunk, S;
   float scale_log2;
+  uint64_t wait_ns;    // bound of every device wait (SPEC_WAIT_NS unless a test lowers it)
+  int withhold_stage;  // -1; a test sets a K/V stage whose arrival the copy warps withhold
 };
 
 // The tcgen05 partial pass: rows_per_cta (128 or 256) query rows of one KV head

@@ -105,7 +105,7 @@ SPEC_DEV void copy_stages(const AttnParams& p, const Chunk& ch, uint8_t* stages,
   const int pshift = __ffs(P) - 1;
   for (int k = 0; k < ch.nst; ++k) {
     const int slot = k % NS;
-    if (k >= NS && !mbar_wait(&kv_empty[slot], ((k / NS) - 1) & 1, p.err)) break;
+    if (k >= NS && !mbar_wait(&kv_empty[slot], ((k / NS) - 1) & 1, p.err, p.wait_ns)) break;
     const uint32_t sbase = smem_u32(stages + slot * kStageBytes);
 #pragma unroll 4
     for (int jt = 0; jt < kST / kTokLanes; ++jt) {
@@ -133,9 +133,10 @@ SPEC_DEV void copy_stages(const AttnParams& p, const Chunk& ch, uint8_t* stages,
       }
     }
     // the stage's barrier counts this thread once its copies have landed
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
-                     smem_u32(&kv_full[slot]))
-                 : "memory");
+    if (k != p.withhold_stage)  // (a test can withhold one stage: its waiters time out)
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                       smem_u32(&kv_full[slot]))
+                   : "memory");
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncwarp();
@@ -367,15 +368,15 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
     copy_stages<kStages>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, p.err);
+      bool ok = mbar_wait(q_full, 0, p.err, p.wait_ns);
       tc_fence_after();
       for (int j = 0; ok && j <= nst; ++j) {
         if (j < nst) {  // S(j) = Q K_j^T into score buffer j & 1
           const int slot = j % kStages;
-          if (!mbar_wait(&kv_full[slot], (j / kStages) & 1, p.err)) break;
+          if (!mbar_wait(&kv_full[slot], (j / kStages) & 1, p.err, p.wait_ns)) break;
           fence_proxy_async();  // the copy warps' generic-proxy writes, seen by the tensor cores
           // the buffer held P(j - 2): PV(j - 2) must have read it
-          if (j >= 2 && !mbar_wait(o_done, (j - 2) & 1, p.err)) break;
+          if (j >= 2 && !mbar_wait(o_done, (j - 2) & 1, p.err, p.wait_ns)) break;
           tc_fence_after();
           mma_scores(tmem + kColS + (j & 1) * kST, true, tmem + kColQ, 0,
                      smem_u32(stages + slot * kStageBytes));
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
         if (j >= 1) {  // O += P(j-1) V_{j-1}
           const int jj = j - 1;
           const int slot = jj % kStages;
-          if (!mbar_wait(p_full, jj & 1, p.err)) break;
+          if (!mbar_wait(p_full, jj & 1, p.err, p.wait_ns)) break;
           tc_fence_after();
           mma_pv(tmem + kColO, tmem + kColS + (jj & 1) * kST,
                  smem_u32(stages + slot * kStageBytes) + 2 * kHalf, jj == 0);
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
         }
       }
       tc_commit(mma_done);  // every issued MMA completes before tensor memory is freed
-      mbar_wait(mma_done, 0, p.err);
+      mbar_wait(mma_done, 0, nullptr);  // never cut short: TMEM is freed next
     }
     __syncwarp();
   } else {
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
     RowState st;
     bool ok = true;
     for (int j = 0; j < nst && ok; ++j) {
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err)) {
+      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -429,12 +430,12 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
       if (warp_live)
         ok = softmax_tile(p, st, lane_base + kColS + (j & 1) * kST, o_addr, ch.c0 + j * kST,
                           ch.ctx, w, j == 0,
-                          [&]() { return mbar_wait(o_done, (j - 1) & 1, p.err); });
+                          [&]() { return mbar_wait(o_done, (j - 1) & 1, p.err, p.wait_ns); });
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && mbar_wait(o_done, (nst - 1) & 1, p.err)) {
+    if (ok && mbar_wait(o_done, (nst - 1) & 1, p.err, p.wait_ns)) {
       tc_fence_after();
       if (warp_live) write_partial(p, ch, st, o_addr, rho, valid);
     }
@@ -516,17 +517,17 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
     copy_stages<kStages>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, p.err);
+      bool ok = mbar_wait(q_full, 0, p.err, p.wait_ns);
       tc_fence_after();
       const uint32_t q0 = smem_u32(qs);
       for (int j = 0; ok && j < nst; ++j) {
         const int slot = j % kStages;
-        if (!mbar_wait(&kv_full[slot], (j / kStages) & 1, p.err)) break;
+        if (!mbar_wait(&kv_full[slot], (j / kStages) & 1, p.err, p.wait_ns)) break;
         fence_proxy_async();  // the copy warps' generic-proxy writes, seen by the tensor cores
         const uint32_t kb = smem_u32(stages + slot * kStageBytes);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {  // S_m(j) once PV_m(j-1) has read P_m(j-1)
-          if (j >= 1 && !mbar_wait(&o_done[m], (j - 1) & 1, p.err)) {
+          if (j >= 1 && !mbar_wait(&o_done[m], (j - 1) & 1, p.err, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
         if (!ok) break;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {  // O_m += P_m(j) V_j
-          if (!mbar_wait(&p_full[m], j & 1, p.err)) {
+          if (!mbar_wait(&p_full[m], j & 1, p.err, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
         tc_commit(&kv_empty[slot]);  // the stage is free once these MMAs complete
       }
       tc_commit(mma_done);  // every issued MMA completes before tensor memory is freed
-      mbar_wait(mma_done, 0, p.err);
+      mbar_wait(mma_done, 0, nullptr);  // never cut short: TMEM is freed next
     }
     __syncwarp();
   } else {
@@ -583,19 +584,19 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
     RowState st;
     bool ok = true;
     for (int j = 0; j < nst && ok; ++j) {
-      if (!mbar_wait(&s_full[m], j & 1, p.err)) {
+      if (!mbar_wait(&s_full[m], j & 1, p.err, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (warp_live)
         ok = softmax_tile(p, st, s_addr, o_addr, ch.c0 + j * kST, ch.ctx, w, j == 0,
-                          [&]() { return mbar_wait(&o_done[m], (j - 1) & 1, p.err); });
+                          [&]() { return mbar_wait(&o_done[m], (j - 1) & 1, p.err, p.wait_ns); });
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[m]);
     }
-    if (ok && mbar_wait(&o_done[m], (nst - 1) & 1, p.err)) {
+    if (ok && mbar_wait(&o_done[m], (nst - 1) & 1, p.err, p.wait_ns)) {
       tc_fence_after();
       if (warp_live) write_partial(p, ch, st, o_addr, rho, valid);
     }

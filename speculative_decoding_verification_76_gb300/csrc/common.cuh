@@ -83,10 +83,12 @@ SPEC_DEV bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity, uint32_t ns) {
 }
 
 // Bounded wait: returns false (and records an error) if the phase does not
-// complete within SPEC_WAIT_NS.  The fast path touches no global memory: it
-// polls with suspended waits; only a wait that has already lasted long checks
-// the clock and whether another wait of this launch has given up.
-SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+// complete within limit_ns (SPEC_WAIT_NS unless a test lowers it).  The fast
+// path touches no global memory: it polls with suspended waits; only a wait
+// that has already lasted long checks the clock and whether another wait of
+// this launch has given up.
+SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                        uint64_t limit_ns = SPEC_WAIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   for (int it = 0; it < 64; ++it)
     if (mbar_try_wait_ns(bar, parity, 1000)) return true;
@@ -96,7 +98,7 @@ SPEC_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
     if (err && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
     for (int it = 0; it < 256; ++it)
       if (mbar_try_wait_ns(bar, parity, 1000)) return true;
-    if (global_ns() - t0 > SPEC_WAIT_NS) break;
+    if (global_ns() - t0 > limit_ns) break;
   }
   set_error(err, SPEC_ERR_MBAR_TIMEOUT);
   return false;

@@ -154,3 +154,9 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(api, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         api.load(str(tmp_path / "missing.so"))
+
+
+def test_debug_fault_setting_host_checks(lib):
+    assert lib.spec_debug_attn_fault(-2, 0) == api.SPEC_EINVAL
+    assert lib.spec_debug_attn_fault(3, 1000) == api.SPEC_OK
+    assert lib.spec_debug_attn_fault(-1, 0) == api.SPEC_OK     # restored
