@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kSoftWarps);
+    mbar_init(p_full, 1);  // one arrival per tile, after the tile's named barrier
     mbar_init(o_done, 1);
     mbar_init(q_full, 1);
     mbar_init(mma_done, 1);
@@ -419,21 +419,22 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
     const uint32_t o_addr = lane_base + kColO;
     RowState st;
     bool ok = true;
-    for (int j = 0; j < nst && ok; ++j) {
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err, p.wait_ns)) {
-        ok = false;
-        break;
-      }
+    for (int j = 0; j < nst; ++j) {
+      if (ok && !mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err, p.wait_ns)) ok = false;
       tc_fence_after();
       // (rows no output needs have a zero Q, so their scores -- read as P by the
       // PV MMA -- are zero)
-      if (warp_live)
+      if (ok && warp_live)
         ok = softmax_tile(p, st, lane_base + kColS + (j & 1) * kST, o_addr, ch.c0 + j * kST,
                           ch.ctx, w, j == 0,
                           [&]() { return mbar_wait(o_done, (j - 1) & 1, p.err, p.wait_ns); });
+      // all four warps have stored P(j) before it is signalled: a warp that is
+      // done early must not start tile j + 1 (whose scores may be ready) and
+      // signal again.  Every thread passes here on every tile, even after a
+      // wait ran out, so the barrier cannot strand the others.
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kSoftWarps) : "memory");
+      if (threadIdx.x == 0) mbar_arrive(p_full);
     }
     if (ok && mbar_wait(o_done, (nst - 1) & 1, p.err, p.wait_ns)) {
       tc_fence_after();
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&s_full[m], 1);
-      mbar_init(&p_full[m], 4);
+      mbar_init(&p_full[m], 1);  // one arrival per tile, after the tile's named barrier
       mbar_init(&o_done[m], 1);
     }
     mbar_init(q_full, 1);
@@ -583,18 +584,20 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
     const uint32_t o_addr = lane_base + kColO + m * 128;
     RowState st;
     bool ok = true;
-    for (int j = 0; j < nst && ok; ++j) {
-      if (!mbar_wait(&s_full[m], j & 1, p.err, p.wait_ns)) {
-        ok = false;
-        break;
-      }
+    for (int j = 0; j < nst; ++j) {
+      if (ok && !mbar_wait(&s_full[m], j & 1, p.err, p.wait_ns)) ok = false;
       tc_fence_after();
-      if (warp_live)
+      if (ok && warp_live)
         ok = softmax_tile(p, st, s_addr, o_addr, ch.c0 + j * kST, ch.ctx, w, j == 0,
                           [&]() { return mbar_wait(&o_done[m], (j - 1) & 1, p.err, p.wait_ns); });
+      // the tile's four warps have stored P_m(j) before it is signalled (see the
+      // one-tile kernel); every thread passes here on every tile
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[m]);
+      if (m == 0)
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+      else
+        asm volatile("bar.sync 4, 128;" ::: "memory");
+      if (quarter == 0 && lane == 0) mbar_arrive(&p_full[m]);
     }
     if (ok && mbar_wait(&o_done[m], (nst - 1) & 1, p.err, p.wait_ns)) {
       tc_fence_after();

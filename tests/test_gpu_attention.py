@@ -85,6 +85,12 @@ CASES = [
     ("tree64_gqa8", 2, 16, 2, 64, True, (200, 450), 16, (0, 1, 3)),
     ("tree12_gqa4", 3, 8, 2, 12, True, (0, 130), 16, (0, 2)),
     ("ctx0", 2, 8, 2, 5, False, (0, 0), 16, (0,)),
+    # tcgen05 passes with softmax warps that own no valid row: 96 rows (one tile,
+    # a dead warp), 200 rows (two tiles, the second partly dead), 384 rows (the
+    # last CTA's second tile entirely dead)
+    ("tc1_96rows", 2, 16, 2, 12, True, (300, 900), 16, (0, 2)),
+    ("tc2_200rows", 2, 16, 2, 25, True, (300, 900), 16, (0, 3)),
+    ("tc2_384rows", 1, 16, 2, 48, True, (700, 700), 16, (0, 1)),
 ]
 
 
