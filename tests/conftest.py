@@ -27,20 +27,24 @@ def golden():
 
 def pytest_terminal_summary(terminalreporter):
     """Report the flagged-draw counts of the sampler parity comparisons: draws
-    within 1e-5 of a decision threshold, which the bit-exact check skips."""
+    within 1e-5 of a decision threshold, and how many of those sequences came
+    out differently on the GPU (the exact check covers all the others)."""
     from tests.util import FLAG_LOG
     if not FLAG_LOG:
         return
-    tot_f = sum(f for _, f, _ in FLAG_LOG)
-    tot_n = sum(n for _, _, n in FLAG_LOG)
+    tot_f = sum(e[1] for e in FLAG_LOG)
+    tot_n = sum(e[2] for e in FLAG_LOG)
+    tot_d = sum(e[3] for e in FLAG_LOG)
     tr = terminalreporter
-    tr.write_sep("-", f"flagged draws: {tot_f} of {tot_n} sequences in {len(FLAG_LOG)} comparisons")
+    tr.write_sep("-", f"flagged draws: {tot_f} of {tot_n} sequences flagged, {tot_d} of them "
+                      f"differ, in {len(FLAG_LOG)} comparisons")
     by_test = {}
-    for label, f, n in FLAG_LOG:
-        a = by_test.setdefault(label, [0, 0, 0])
+    for label, f, n, d in FLAG_LOG:
+        a = by_test.setdefault(label, [0, 0, 0, 0])
         a[0] += f
         a[1] += n
-        a[2] += 1
-    for label, (f, n, c) in sorted(by_test.items()):
+        a[2] += d
+        a[3] += 1
+    for label, (f, n, d, c) in sorted(by_test.items()):
         if f:
-            tr.write_line(f"  {label}: {f} flagged of {n} ({c} comparisons)")
+            tr.write_line(f"  {label}: {f} flagged of {n}, {d} differ ({c} comparisons)")

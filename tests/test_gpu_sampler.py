@@ -19,7 +19,7 @@ import speculative_decoding_verification_76_gb300 as sv
 from oracle.sampler import SamplerCfg
 from speculative_decoding_verification_76_gb300 import workloads as wl
 from tests.conftest import load_golden
-from tests.util import FLAG_CAP, P_RTOL, cfg_of, record_flags
+from tests.util import P_RTOL, cfg_of, record_flags
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -49,20 +49,33 @@ def run_tree(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=True):
 def compare(gpu, ref, tree=False, max_flagged=None):
     """Bit-exact accepted_len / emitted (and path) on every unflagged sequence.
 
-    The flagged count is recorded for the end-of-run report and capped: at most
-    FLAG_CAP of the sequences (at least one) unless a test constructs
-    near-threshold rows on purpose and passes its own cap."""
+    Flagged sequences (a decision within 1e-5 of its threshold) are compared
+    too: fp32 rounding moves a decision only when it lands far closer to the
+    threshold than the flag margin, so at most a quarter of them (and at least
+    one) may differ -- a kernel that diverged near thresholds fails here.  The
+    flagged count is recorded for the end-of-run report and held under a sanity
+    cap (half the batch) unless a test constructs near-threshold rows on purpose
+    and passes its own."""
     B = len(ref["flagged"])
-    n_flag = int(ref["flagged"].sum())
-    record_flags(os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], n_flag, B)
-    cap = max(1, int(FLAG_CAP * B)) if max_flagged is None else max_flagged
+    fl = np.asarray(ref["flagged"], dtype=bool)
+    n_flag = int(fl.sum())
+    diff = (gpu["accepted_len"] != ref["accepted_len"]) | \
+        (gpu["emitted"] != ref["emitted"]).any(axis=1)
+    if tree:
+        diff |= (gpu["path"] != ref["path"]).any(axis=1)
+    n_flag_diff = int((diff & fl).sum())
+    record_flags(os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], n_flag, B,
+                 n_flag_diff)
+    cap = max(1, B // 2) if max_flagged is None else max_flagged
     assert n_flag <= cap, f"{n_flag} of {B} sequences flagged (cap {cap})"
-    ok = ~ref["flagged"]
+    ok = ~fl
     np.testing.assert_array_equal(gpu["accepted_len"][ok], ref["accepted_len"][ok])
     np.testing.assert_array_equal(gpu["emitted"][ok], ref["emitted"][ok])
     if tree:
         np.testing.assert_array_equal(gpu["path"][ok], ref["path"][ok])
-    # flagged sequences: still a valid outcome (accepted prefix of the drafts)
+    assert n_flag_diff <= max(1, n_flag // 4), \
+        f"{n_flag_diff} of {n_flag} flagged sequences differ from the oracle"
+    # every sequence still has a valid outcome (accepted prefix of the drafts)
     assert (gpu["accepted_len"] >= 0).all()
     return n_flag
 

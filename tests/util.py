@@ -9,15 +9,15 @@ from speculative_decoding_verification_76_gb300 import workloads as wl
 BF16_ATOL = 2e-2     # attention, bf16 inputs, fp32 accumulation (stated tolerance)
 F32_ATOL = 1e-5      # attention, fp32 tiny configuration (stated tolerance)
 P_RTOL = 1e-6        # target distribution p, relative (stated tolerance)
-FLAG_CAP = 0.02      # flagged sequences allowed per comparison (fraction of B, at least 1)
 
-# (test, flagged sequences, sequences) of every sampler comparison in this session;
-# printed at the end of the run by the conftest summary hook
+# (test, flagged sequences, sequences, flagged sequences whose GPU outcome differs)
+# of every sampler comparison in this session; printed at the end of the run by
+# the conftest summary hook
 FLAG_LOG = []
 
 
-def record_flags(label: str, flagged: int, total: int):
-    FLAG_LOG.append((label, int(flagged), int(total)))
+def record_flags(label: str, flagged: int, total: int, flagged_diff: int = 0):
+    FLAG_LOG.append((label, int(flagged), int(total), int(flagged_diff)))
 
 
 def np_u64(t: torch.Tensor) -> np.ndarray:
