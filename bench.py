@@ -199,7 +199,10 @@ class GpuStep:
         w = wl.make_workload(spec, seed=seed, device=device)
         self.w = w
         B, R = spec.B, spec.R
-        self.anc = torch.empty((B, R), dtype=torch.int64, device=device)
+        # a chain needs no ancestor masks: the attention takes none (row i sees
+        # block rows 0 .. i) and no tree_prepare launch is made
+        self.anc = torch.empty((B, R), dtype=torch.int64, device=device) if spec.is_tree \
+            else None
         self.pos = torch.empty((B, R), dtype=torch.int32, device=device)
         self.tst = torch.empty((B,), dtype=torch.int32, device=device)
         self.attn = sv.AttnCall(w.q, w.k_cache, w.v_cache, w.block_table, w.ctx_len, self.anc,
@@ -216,7 +219,7 @@ class GpuStep:
         self.side = torch.cuda.Stream(device=device)
         self.fork = torch.cuda.Event()
         self.join = torch.cuda.Event()
-        self.launches_per_step = 4
+        self.launches_per_step = 4 if spec.is_tree else 3
 
     def sample(self):
         sv, w = self.sv, self.w
@@ -242,7 +245,9 @@ class GpuStep:
                 if ev is not None:
                     ev[3].record(self.side)
             self.join.record(self.side)
-        sv.tree_prepare(w.parent, w.ctx_len, anc_mask=self.anc, pos_ids=self.pos, status=self.tst)
+        if self.spec.is_tree:
+            sv.tree_prepare(w.parent, w.ctx_len, anc_mask=self.anc, pos_ids=self.pos,
+                            status=self.tst)
         if ev is not None:
             ev[0].record(main)
         self.attn.partials()
@@ -483,7 +488,7 @@ def bench_e2e(step: GpuStep, spec, n, ws, dev):
     def one():
         for k in names:
             dst[k].copy_(host[k], non_blocking=True)
-        anc, _, _ = sv.tree_prepare(dst["parent"], dst["ctx_len"])
+        anc = sv.tree_prepare(dst["parent"], dst["ctx_len"])[0] if spec.is_tree else None
         sv.verify_attn(dst["q"], w.k_cache, w.v_cache, dst["block_table"], dst["ctx_len"], anc,
                        num_splits=spec.num_splits, workspace=step.attn.workspace)
         if spec.is_tree:
@@ -614,7 +619,7 @@ def parity_sample(spec, step, w, max_seqs=16):
     decisions of up to max_seqs sequences (bit-exact except flagged draws) and
     attention of two sequences (every row, one query head per KV head)."""
     import oracle
-    from tests.util import cfg_of, np_u64, oracle_attention
+    from tests.util import cfg_of, oracle_attention
     B = spec.B
     seqs = list(range(min(B, max_seqs)))
     sl = slice(0, len(seqs))
@@ -631,7 +636,7 @@ def parity_sample(spec, step, w, max_seqs=16):
     g_emit = step.sout["emitted"].cpu().numpy()[sl]
     ok = ~ref["flagged"]
     mism = int(((g_acc != ref["accepted_len"]) | (g_emit != ref["emitted"]).any(1))[ok].sum())
-    anc = np_u64(step.anc)
+    anc, _, _ = oracle.tree.tree_prepare(w.parent.numpy(), w.ctx_len.numpy())
     G = spec.Hq // spec.Hkv
     heads = [k * G + k % G for k in range(spec.Hkv)]
     bs = list(range(min(B, 2)))

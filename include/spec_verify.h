@@ -108,7 +108,9 @@ spec_status spec_tree_prepare(const int32_t* parent, const int32_t* ctx_len, int
  *              past the sequence's last page are not read.
  *   ctx_len    [B] int32: committed positions, all visible to every row.
  *   anc_mask   [B,R] uint64: block position ctx+j is visible to row i iff bit
- *              j of anc_mask[b,i] is set (spec_tree_prepare's output).
+ *              j of anc_mask[b,i] is set (spec_tree_prepare's output).  NULL
+ *              means a chain: row i sees block rows 0 .. i (the causal block,
+ *              no spec_tree_prepare launch needed).
  *   scale      softmax scale; <= 0 selects 1/sqrt(D).
  *   num_splits KV chunks per (sequence, KV head); 0 lets the library choose.
  *   workspace  >= spec_verify_attn_workspace_size(...) bytes, 256-B aligned.

@@ -305,7 +305,8 @@ def verify_attn(q, k_cache, v_cache, block_table, ctx_len, anc_mask, scale: floa
     _need(v_cache, "v_cache", dt, k_cache.shape)
     _need(block_table, "block_table", torch.int32)
     _need(ctx_len, "ctx_len", torch.int32, (B,))
-    _need(anc_mask, "anc_mask", torch.int64, (B, R))
+    if anc_mask is not None:          # None: a chain (row i sees block rows 0 .. i)
+        _need(anc_mask, "anc_mask", torch.int64, (B, R))
     maxp = block_table.shape[1]
     if workspace is None:
         workspace = new_workspace(attn_workspace_size(B, R, Hq, Hkv, D, P, maxp, num_splits),
@@ -340,7 +341,8 @@ class AttnCall:
         _need(v_cache, "v_cache", dt, k_cache.shape)
         _need(block_table, "block_table", torch.int32)
         _need(ctx_len, "ctx_len", torch.int32, (B,))
-        _need(anc_mask, "anc_mask", torch.int64, (B, R))
+        if anc_mask is not None:      # None: a chain
+            _need(anc_mask, "anc_mask", torch.int64, (B, R))
         maxp = block_table.shape[1]
         self.workspace = workspace if workspace is not None else new_workspace(
             attn_workspace_size(B, R, Hq, Hkv, D, P, maxp, num_splits), q.device)

@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
   const int rho0 = rt * RT + rg * 16 + r0;
   const int rho1 = rho0 + 8;
   const bool v0 = rho0 < p.RG, v1 = rho1 < p.RG;
-  const uint64_t w0 = v0 ? p.anc_mask[(size_t)b * p.R + rho0 / p.G] : 0ull;
-  const uint64_t w1 = v1 ? p.anc_mask[(size_t)b * p.R + rho1 / p.G] : 0ull;
+  const uint64_t w0 = v0 ? attn::row_mask(p, b, rho0 / p.G) : 0ull;
+  const uint64_t w1 = v1 ? attn::row_mask(p, b, rho1 / p.G) : 0ull;
   const int tsb = tg * TS;            // first token of this warp's sub-block
 
   const uint32_t q_base = smem_u32(qs);
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const AttnParams p) {
     const int rho = rbase + warp;
     const bool live = rho < p.RG;
     const int i = live ? rho / p.G : 0, g = live ? rho % p.G : 0;
-    const uint64_t w = live ? p.anc_mask[(size_t)b * p.R + i] : 0ull;
+    const uint64_t w = live ? attn::row_mask(p, b, i) : 0ull;
     if (live)
       for (int d = lane; d < D; d += 32)
         qsh[warp][d] = p.qf[(((size_t)b * p.R + i) * p.Hq + (size_t)kvh * p.G + g) * D + d];
@@ -697,7 +697,7 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
                              float scale, int num_splits, void* workspace, size_t workspace_bytes,
                              void* out, float* lse_out, void* stream, int phase) {
   if (!ctx_len || !workspace) return SPEC_EINVAL;
-  if ((phase & kPartials) && (!q || !k_cache || !v_cache || !block_table || !anc_mask))
+  if ((phase & kPartials) && (!q || !k_cache || !v_cache || !block_table))
     return SPEC_EINVAL;
   if ((phase & kCombine) && !out) return SPEC_EINVAL;
   if (B < 0 || R < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || page_size < 1 || num_pages < 1 ||
@@ -751,6 +751,7 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   prm.scale_log2 = sc * kLog2e;
   prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   prm.withhold_stage = g_withhold_stage.load(std::memory_order_relaxed);
+
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (phase & kPartials) {

@@ -30,6 +30,13 @@ struct AttnParams {
   int withhold_stage;  // -1; a test sets a K/V stage whose arrival the copy warps withhold
 };
 
+// The visibility word of block row i of sequence b: the caller's ancestor mask,
+// or for a chain (no mask given) rows 0 .. i.
+SPEC_DEV uint64_t row_mask(const AttnParams& p, int b, int i) {
+  if (p.anc_mask) return p.anc_mask[(size_t)b * p.R + i];
+  return i >= 63 ? ~0ull : ((2ull << i) - 1ull);
+}
+
 // The tcgen05 partial pass: rows_per_cta (128 or 256) query rows of one KV head
 // per CTA, 128-token stages, grid (Hkv * row_tiles, S, B).  Defined in
 // attn_tc.cu.

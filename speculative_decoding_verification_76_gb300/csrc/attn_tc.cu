@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
     if (threadIdx.x == 0) mbar_arrive(q_full);
 
-    const uint64_t w = valid ? p.anc_mask[(size_t)ch.b * p.R + rho / p.G] : 0ull;
+    const uint64_t w = valid ? attn::row_mask(p, ch.b, rho / p.G) : 0ull;
     const uint32_t o_addr = lane_base + kColO;
     RowState st;
     bool ok = true;
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
     if (threadIdx.x == 0) mbar_arrive(q_full);
 
-    const uint64_t w = valid ? p.anc_mask[(size_t)ch.b * p.R + rho / p.G] : 0ull;
+    const uint64_t w = valid ? attn::row_mask(p, ch.b, rho / p.G) : 0ull;
     const uint32_t s_addr = lane_base + kColS + m * kST;
     const uint32_t o_addr = lane_base + kColO + m * 128;
     RowState st;

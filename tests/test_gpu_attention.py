@@ -124,6 +124,21 @@ def test_chain_parent_null_equals_explicit_chain():
     assert np.array_equal(a[0], b[0])
 
 
+@pytest.mark.parametrize("Hq,Hkv,R", [(8, 2, 7), (64, 8, 16), (4, 1, 64)])
+def test_attention_without_mask_is_the_chain(Hq, Hkv, R):
+    """No ancestor mask = the causal chain: identical outputs to the explicit chain
+    mask on every bf16 kernel (warp-MMA: 28 rows per KV head; tcgen05 one tile:
+    128; two tiles: 256)."""
+    spec = wl.Spec("c2", B=2, Hq=Hq, Hkv=Hkv, D=128, V=16, ctx=(150, 700), gamma=R - 1,
+                   shuffle_pages=True, seed=R)
+    g = wl.make_attention_inputs(spec, device=DEV)
+    anc, _, _ = sv.tree_prepare(None, g.ctx_len, R=R)
+    o1, l1 = sv.verify_attn(g.q, g.k_cache, g.v_cache, g.block_table, g.ctx_len, anc)
+    o2, l2 = sv.verify_attn(g.q, g.k_cache, g.v_cache, g.block_table, g.ctx_len, None)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_invisible_nodes_and_stale_cache_do_not_leak():
     """Sibling nodes' K/V and cache slots past the sequence end must not matter."""
     spec = wl.Spec("fox", B=1, Hq=4, Hkv=1, D=128, V=16, ctx=(70, 70), tree_nodes=6, seed=5)
