@@ -244,7 +244,21 @@ typedef struct {
   int32_t eos_id;
 } spec_sampler;
 
+/* Workspace of spec_accept_sample / _tree for B sequences of R rows (N
+ * nodes) over a vocabulary of V; 0 for invalid sizes.
+ *
+ * When many rows are sampled at once (B R cluster(V) > 2 x the SM count,
+ * cluster(V) = min(8, ceil(V / 16384))) with truncation, each row is handled
+ * by one CTA that sweeps it twice (maximum, then Z and a candidate list).
+ * A workspace of spec_accept_sample_workspace_size_two_pass(B, R, V) bytes
+ * (about 260 KB per row more) selects the two-pass variant instead: a
+ * pre-pass sweeps every row from HBM once over all SMs (maximum, Z and the
+ * candidate list of each warp range), then one CTA per row finishes it.  The
+ * results are the same.  Alone the two-pass variant is slightly faster; next
+ * to concurrent HBM-bound work (the verify step's attention) the one-kernel
+ * variant is, so it is the default. */
 size_t spec_accept_sample_workspace_size(int B, int R, int V);
+size_t spec_accept_sample_workspace_size_two_pass(int B, int R, int V);
 
 /* ------------------------------------------------------------------------
  * spec_accept_sample -- chain verification of B sequences.

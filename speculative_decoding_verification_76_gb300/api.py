@@ -26,6 +26,7 @@ EXPORTS = (
     "spec_status_str", "spec_tree_prepare", "spec_verify_attn_workspace_size",
     "spec_verify_attn_num_splits", "spec_verify_attn", "spec_verify_attn_partials",
     "spec_verify_attn_combine", "spec_accept_sample_workspace_size",
+    "spec_accept_sample_workspace_size_two_pass",
     "spec_accept_sample", "spec_accept_sample_tree", "spec_workspace_error",
     "spec_kv_commit", "spec_verify_attn_noalloc", "spec_verify_attn_noalloc_error",
     "spec_append_block", "spec_logits_penalize", "spec_debug_attn_fault",
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_attn_combine.argtypes = common + [_P, _P, _P]
     lib.spec_accept_sample_workspace_size.restype = _SZ
     lib.spec_accept_sample_workspace_size.argtypes = [_I, _I, _I]
+    lib.spec_accept_sample_workspace_size_two_pass.restype = _SZ
+    lib.spec_accept_sample_workspace_size_two_pass.argtypes = [_I, _I, _I]
     lib.spec_accept_sample.restype = _I
     lib.spec_accept_sample.argtypes = [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(_Sampler), _P,
                                        _SZ, _P, _P, _P, _P, _P]
@@ -373,7 +376,11 @@ class AttnCall:
 
 
 # ------------------------------------------------------------------ sampler
-def sample_workspace_size(B, R, V) -> int:
+def sample_workspace_size(B, R, V, two_pass: bool = False) -> int:
+    """Bytes of sampler workspace; two_pass: room for the two-pass streaming
+    variant (many truncated rows), which a workspace of that size selects."""
+    if two_pass:
+        return int(load().spec_accept_sample_workspace_size_two_pass(B, R, V))
     return int(load().spec_accept_sample_workspace_size(B, R, V))
 
 

@@ -70,6 +70,13 @@ struct Outcome {
   int32_t flags;   // 1 if the row's logits are not finite
 };
 
+// Per warp range of a row, from the streaming pre-pass (many-row sampling).
+struct RangeStat {
+  float m;       // maximum of the range's logits (NaN-propagating; -inf if all are -inf)
+  float zh, zl;  // Z of the range relative to its finite maximum, as a float pair
+  int32_t cnt;   // ids at or above the row's candidate floor (> kSWCap: not all stored)
+};
+
 struct SP {
   const float* logits;
   const float* q;
@@ -89,6 +96,12 @@ struct SP {
   int32_t* path;
   float* p_out;
   int32_t* status;
+  // streaming pre-pass results (nullptr: the row kernel sweeps the row itself)
+  RangeStat* stats;   // [rows][32]
+  float* lfloor;      // [rows][2]: candidate floor as a logit (+inf: no lists), samples' maximum
+  int32_t* lid_g;     // [rows][32][kSwW][kSegCap] listed ids per range segment, ascending
+  float* lval_g;      // [rows][32][kSwW][kSegCap] their logits
+  int32_t* segcnt;    // [rows][32][kSwW] ids listed per segment
 };
 
 // One CTA's contribution to a cluster exchange (32 bytes).
@@ -129,6 +142,7 @@ struct Sh {
   float invw_used[kMaxN];
   Outcome outs[kMaxN];
   int cpos[kMaxN];  // list position of each child's token (-1: not kept)
+  float zpre[2];    // Z as a float pair, from the streaming pre-pass
   float eprobe;
   int token_in;
   uint64_t bar;
@@ -638,12 +652,39 @@ SPEC_DEV Sel radix_select(const float* lrow, int n, bool target_is_fraction, dou
       rs.rcnt[h * 256 + i] = 0u;
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < n; k += NT) {
-      const uint32_t key = okey(__ldg(lrow + k));
-      if ((key & pmask) == prefix && keep(k, key)) {
-        const uint32_t digit = (key >> shift) & 255u;
-        atomicAdd(&rs.rcnt[h * 256 + digit], 1u);
-        atomicAdd(&rs.rmass[h * 256 + digit], weight(k));
+    // the lanes of a warp that share a digit add their counts and weights
+    // first (weights < 2^41: two 32-bit partial sums), one shared atomic per
+    // digit and warp: the keys of a row crowd into a few digits
+    const int lane = threadIdx.x & 31;
+    constexpr int U = 8;  // logits in flight per thread
+    for (int k0 = threadIdx.x - lane; k0 < n; k0 += U * NT) {  // warp-uniform
+      float lv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * NT + lane;
+        lv[u] = k < n ? __ldg(lrow + k) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * NT + lane;
+        uint32_t label = 0xFFFFFFFFu;
+        unsigned long long wt = 0;
+        if (k < n) {
+          const uint32_t key = okey(lv[u]);
+          if ((key & pmask) == prefix && keep(k, key)) {
+            label = (key >> shift) & 255u;
+            wt = weight(k);
+          }
+        }
+        const unsigned grp = __match_any_sync(kFull, label);
+        if (label != 0xFFFFFFFFu) {
+          const uint32_t hi = __reduce_add_sync(grp, (uint32_t)(wt >> 24));
+          const uint32_t lo = __reduce_add_sync(grp, (uint32_t)(wt & 0xFFFFFFull));
+          if (lane == __ffs(grp) - 1) {
+            atomicAdd(&rs.rcnt[h * 256 + label], (uint32_t)__popc(grp));
+            atomicAdd(&rs.rmass[h * 256 + label], ((unsigned long long)hi << 24) + lo);
+          }
+        }
       }
     }
     __syncthreads();
@@ -697,12 +738,18 @@ SPEC_DEV Sel radix_select(const float* lrow, int n, bool target_is_fraction, dou
 template <int NT, class Pred>
 SPEC_DEV int nth_in_cluster(int n, int lo, int nth, Pred pred, int rank, int CS, int& ph,
                             Sh<NT / 32>& sh) {
-  const int seg = (n + NT - 1) / NT;
-  const int s0 = min((int)threadIdx.x * seg, n), s1 = min(s0 + seg, n);
-  int c = 0;
-  for (int k = s0; k < s1; ++k) c += pred(k) ? 1 : 0;
+  // each warp counts one contiguous range of ids, 32 consecutive ids per step
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = ((n + NW - 1) / NW + 31) / 32 * 32;
+  const int s0 = min(warp * seg, n), s1 = min(s0 + seg, n);
+  int c = 0;  // warp-uniform
+  for (int k0 = s0; k0 < s1; k0 += 32) {
+    const int k = k0 + lane;
+    c += __popc(__ballot_sync(kFull, k < s1 && pred(k)));
+  }
   int tot;
-  const int excl = block_excl_scan_i<NT>(c, &tot, sh);
+  const int excl = __shfl_sync(kFull, block_excl_scan_i<NT>(lane == 0 ? c : 0, &tot, sh), 0);
   exchange(Post{{(unsigned long long)tot, 0ull, 0ull, 0ull}}, CS, ph, sh);
   int before = 0, owner = -1;
   for (int r = 0; r < CS; ++r) {
@@ -713,13 +760,18 @@ SPEC_DEV int nth_in_cluster(int n, int lo, int nth, Pred pred, int rank, int CS,
   int found = INT_MAX;
   if (owner == rank) {
     const int local = nth - before;
-    if (excl < local && local <= excl + c) {
+    if (excl < local && local <= excl + c) {  // warp-uniform: this warp holds it
       int cnt = excl;
-      for (int k = s0; k < s1; ++k)
-        if (pred(k) && ++cnt == local) {
-          found = lo + k;
+      for (int k0 = s0; k0 < s1; k0 += 32) {
+        const int k = k0 + lane;
+        unsigned b = __ballot_sync(kFull, k < s1 && pred(k));
+        if (cnt + __popc(b) >= local) {
+          for (int i = cnt + 1; i < local; ++i) b &= b - 1u;  // drop the lower set bits
+          found = lo + k0 + __ffs(b) - 1;
           break;
         }
+        cnt += __popc(b);
+      }
     }
   }
   found = block_min_i<NT>(found, sh);
@@ -904,12 +956,16 @@ SPEC_DEV void find_range(bool topk, bool topp, int top_k, float top_p, unsigned 
 
 // ---------------------------------------------------------------- the cut among the members
 // Threads t < total hold member t (logit key, E bits), unsorted.  Sorts the
-// members by key, descending (= logit desc, id asc), with shuffles inside a
-// warp and shared memory (xkey / xbits, >= NT entries) across warps, then
-// finds the cut on exact masses (units of 2^-44) running from a_lo, the mass
-// above the members: the top-k member kidx (-1: no top-k), then (top-p) the
-// first running mass >= top_p * Z_k.  Returns false if the cut does not lie
-// among the members.
+// members by key, descending (= logit desc, id asc): up to kRankSortMax
+// members by rank (each member counts the larger keys; keys are distinct,
+// the id is part of them), more by a bitonic network (shuffles inside a warp,
+// shared memory across warps; xkey / xbits hold >= NT entries).  Then finds
+// the cut on exact masses (units of 2^-44) running from a_lo, the mass above
+// the members: the top-k member kidx (-1: no top-k), then (top-p) the first
+// running mass >= top_p * Z_k.  Returns false if the cut does not lie among
+// the members.
+constexpr int kRankSortMax = 256;
+
 template <int NT>
 SPEC_DEV bool select_cut(unsigned long long key, uint32_t eb, int total, unsigned long long a_lo,
                          int kidx, bool topp, float top_p, unsigned long long zall_fx,
@@ -918,6 +974,27 @@ SPEC_DEV bool select_cut(unsigned long long key, uint32_t eb, int total, unsigne
   const int t = threadIdx.x;
   int P = 1;
   while (P < total) P <<= 1;
+  if (total <= kRankSortMax) {
+    if (t < total) {
+      xkey[t] = key;
+      xbits[t] = eb;
+    }
+    __syncthreads();
+    int rank = 0;
+    if (t < total)
+      for (int j = 0; j < total; ++j) rank += xkey[j] > key ? 1 : 0;
+    __syncthreads();
+    if (t < total) {
+      xkey[rank] = key;
+      xbits[rank] = eb;
+    }
+    __syncthreads();
+    if (t < total) {
+      key = xkey[t];
+      eb = xbits[t];
+    }
+    P = 0;  // sorted: skip the network
+  }
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       unsigned long long ok2;
@@ -961,7 +1038,7 @@ SPEC_DEV bool select_cut(unsigned long long key, uint32_t eb, int total, unsigne
   if (!topp) {
     if (t == last) pick = t;
   } else {
-    const unsigned long long thr = (unsigned long long)((double)top_p * (double)zk);
+    const unsigned long long thr = mul_frac(zk, top_p);
     if (live && t <= last && incl - mt < thr && incl >= thr) pick = t;
   }
   if (pick >= 0) {  // unique: masses are positive
@@ -1480,6 +1557,9 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
       ensure_kept(true);
       float* dst = p.p_out + (size_t)row * p.V + lo;
       for (int k = threadIdx.x; k < n; k += NT) dst[k] = buf[k] * invz;
+      // every thread has read buf before a residual draw rewrites it in place
+      // (its warps own other elements than this loop's threads)
+      __syncthreads();
     }
 
     const float u_final = u_last;
@@ -1615,7 +1695,24 @@ constexpr int kSCap = 16384;    // list entries per row (kSCap / 32 per warp)
 constexpr int kSBudget = 10240; // candidates a row's floor aims at (sampled estimate)
 constexpr int kSListMaxV = 163840;  // rows up to this long are listed (one flag bit per id)
 
-template <bool FAST>
+// Each warp of the row kernel owns one contiguous range of the row's ids
+// (a multiple of 32 long); the two-pass variant's pre-pass sweeps each such
+// range with one CTA of kSwW warps.
+constexpr int kRangesPerRow = kSNT / 32;
+constexpr int kSwW = 8;
+constexpr int kSwNT = 32 * kSwW;
+constexpr int kSWCap = kSCap / kRangesPerRow;  // list entries a row-kernel warp holds
+constexpr int kSegCap = 128;  // list entries stored per pre-pass warp segment (kSwW per range)
+
+__host__ __device__ inline int stream_range_width(int V) {
+  return ((V + kRangesPerRow - 1) / kRangesPerRow + 31) / 32 * 32;
+}
+constexpr int kSamples = 1024;                 // samples per row for the floor
+static_assert(kSamples == kSNT, "the floor samples are the row kernel's, one per thread");
+
+// PRE: the pre-pass (sampler_sweep_kernel) has swept the row: the maximum, Z
+// and the candidate lists are read from its results, not from the logits.
+template <bool FAST, bool PRE>
 __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   constexpr int NT = kSNT, NW = NT / 32, WCAP = kSCap / NW;
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -1702,7 +1799,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 
   // each warp owns one contiguous id range of the row (a multiple of 32 long);
   // four logits of ids k..k+3 at a time (-inf past the range)
-  const int rw = ((V + NW - 1) / NW + 31) / 32 * 32;
+  const int rw = stream_range_width(V);
   const int r0 = min(warp * rw, V), r1 = min((warp + 1) * rw, V);
   auto load4 = [&](int k, float (&lv)[4]) {
     if (vec && k + 3 < r1) {
@@ -1719,17 +1816,29 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   const unsigned lt = (1u << lane) - 1u;
 
   // ---- 1. maximum (NaN-propagating); one sample per thread, evenly spaced
-  // over the row, for the candidate floor
-  const float smp = trunc ? ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol) : 0.f;
-  float mx = -INFINITY;
-  sweep([&](int, float l) { mx = fmax_nan(mx, l); });
+  // over the row, for the candidate floor.  PRE: every warp combines the
+  // ranges' maxima (lane r holds range r's results)
+  const float smp =
+      (!PRE && trunc) ? ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol) : 0.f;
+  float m;
+  RangeStat st{0.f, 0.f, 0.f, 0};
+  if constexpr (PRE) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the pre-pass has completed
+    st = p.stats[(size_t)row * kRangesPerRow + lane];
+    m = st.m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
-  if (lane == 0) sh.red_f[warp] = mx;
-  __syncthreads();
-  float m = sh.red_f[0];
-  for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.red_f[w]);
-  __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
+  } else {
+    float mx = -INFINITY;
+    sweep([&](int, float l) { mx = fmax_nan(mx, l); });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
+    if (lane == 0) sh.red_f[warp] = mx;
+    __syncthreads();
+    m = sh.red_f[0];
+    for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.red_f[w]);
+    __syncthreads();
+  }
   const bool bad = isnan(m) || m == INFINITY || m == -INFINITY;
   Outcome oc{0, -1, 0, bad ? 1 : 0};
   // the chain test's operands, loaded now: their latency hides under the next sweep
@@ -1758,7 +1867,13 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // sampled count at or above it stays within the list budget; the elements
     // of bins <= bf are listed.  -1: no floor (every element histogrammed)
     int bf = -1;
-    if (trunc && V <= kSListMaxV) {
+    if constexpr (PRE) {
+      // the bins whose every element lies at or above the pre-pass's floor:
+      // those above the bin of E at the floor (taken 2^-12 high, which covers
+      // the rounding of E)
+      const float Lf = p.lfloor[2 * row];
+      if (trunc && Lf < INFINITY) bf = ebin(__float_as_uint(Eof(Lf) * 1.000244140625f)) - 1;
+    } else if (trunc && V <= kSListMaxV) {
       const float budget =
           topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
       const int ns = (int)(budget * (float)NT / (float)V);
@@ -1788,6 +1903,24 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       zc = (t - zs) - y;
       zs = t;
     };
+    if constexpr (PRE) {
+      if (warp == 0) {
+        // Z = sum over the ranges of Z_r E(m_r), in float pairs, fixed order
+        const float sc = st.m == -INFINITY ? 0.f : Eof(st.m);
+        float zh2 = st.zh * sc;
+        float zl2 = __fmaf_rn(st.zh, sc, -zh2) + st.zl * sc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float oh = __shfl_xor_sync(kFull, zh2, o);
+          const float ol = __shfl_xor_sync(kFull, zl2, o);
+          df_acc(zh2, zl2, oh, ol);
+        }
+        if (lane == 0) {
+          sh.zpre[0] = zh2;
+          sh.zpre[1] = zl2;
+        }
+      }
+    } else
     for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
       float lv[4][4];
 #pragma unroll
@@ -1824,7 +1957,57 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     // elements (exactly those of bins <= bf); if a list overflowed, of every
     // element
     int cntw = 0;
-    if (listing) {
+    if (PRE) {
+      // this warp's range list, copied from the pre-pass results: kSwW
+      // segments in order (the entry j of the range lies in the last segment
+      // whose offset is <= j)
+      const int c = __shfl_sync(kFull, st.cnt, warp);
+      cntw = listing ? c : 0;
+      if (listing && c <= WCAP) {
+        const size_t rg = (size_t)row * kRangesPerRow + warp;
+        const int sc = lane < kSwW ? p.segcnt[rg * kSwW + lane] : 0;
+        int incl = sc;
+#pragma unroll
+        for (int o = 1; o < kSwW; o <<= 1) {
+          const int t2 = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        int soff[kSwW];
+#pragma unroll
+        for (int k = 0; k < kSwW; ++k) soff[k] = __shfl_sync(kFull, incl - sc, k);
+        const int32_t* gid = p.lid_g + rg * kSwW * kSegCap;
+        const float* gval = p.lval_g + rg * kSwW * kSegCap;
+        for (int j0 = 0; j0 < c; j0 += 256) {
+          int idv[8];
+          float lvv[8];  // eight entries in flight per lane
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            int sg = 0, so = 0;  // the last segment whose offset is <= j (offsets ascend)
+#pragma unroll
+            for (int k = 1; k < kSwW; ++k)
+              if (soff[k] <= j) {
+                sg = k;
+                so = soff[k];
+              }
+            const int at = sg * kSegCap + (j - so);
+            idv[u] = j < c ? gid[at] : 0;
+            lvv[u] = j < c ? gval[at] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            if (j < c) {
+              lid[warp * WCAP + j] = idv[u];
+              lval[warp * WCAP + j] = lvv[u];
+              const uint32_t bits = __float_as_uint(Eof(lvv[u]));
+              const int bn = ebin(bits);
+              if (bn <= bf) hist(bits, bn);
+            }
+          }
+        }
+      }
+    } else if (listing) {
       __syncwarp();  // the warp's flag words are written
       const int w0 = (r0 + 31) >> 5, w1 = (r1 + 31) >> 5;  // r0: a multiple of 32, or V
       for (int wb = w0; wb < w1; wb += 32) {
@@ -1870,7 +2053,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     const bool fit = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
     // lists hold every element that can be kept (ids, logits)
     bool cand_lists = listing && fit;
-    if (listing && !fit) {
+    if ((listing && !fit) || (PRE && trunc && !listing)) {
       for (int k = threadIdx.x; k < kHist; k += NT) {
         hcnt[k] = 0u;
         hm[k] = 0u;
@@ -1879,10 +2062,26 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       sweep([&](int, float l) { hist_e(Eof(l)); });
       bf = -1;
     }
-    const float zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
-    const float zl = block_sum_f<NT>(-zc, sh);
+    float zh, zl;
+    if constexpr (PRE) {
+      __syncthreads();  // the histogram and the Z pair are complete
+      zh = sh.zpre[0];
+      zl = sh.zpre[1];
+    } else {
+      zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
+      zl = block_sum_f<NT>(-zc, sh);
+    }
     const float e_probe = sh.eprobe;
     const unsigned long long zfx = fx44_pair(zh, zl);  // Z in units of 2^-44
+    // a draft row that is likely to reject (p(x) <= E(x) / Z_kept is not
+    // surely above u q(x)), or a tree node with children, reads q at its kept
+    // ids for the residual: start those reads into L2 now, under the cut
+    if (cand_lists && qrow != nullptr &&
+        (p.tree ? probe >= 0 : (chain_test && !(u_test * q_probe * (zh + zl) < e_probe)))) {
+      const int cnt = sh.list_n[warp];
+      for (int j = lane; j < cnt; j += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lid[warp * WCAP + j]));
+    }
 
     Cut cut{0, 0.f, 0u, INT_MAX};
     float zkept = zh + zl;
@@ -1933,8 +2132,19 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         tmode = f_mode;
         cand_lists = false;
       }
-      const int b_lo = f_lo, b_hi = f_hi, kidx = f_k;
-      if (tmode == 1) {
+      int b_lo = f_lo, b_hi = f_hi, kidx = f_k;
+      // a second attempt one bin wider on each side: the rounded bin masses
+      // may place a cut that lies within their rounding of a bin edge one bin off
+      for (int attempt = 0; tmode == 1 && attempt < 2; ++attempt) {
+        if (attempt == 1) {
+          if (b_lo > 0) {
+            --b_lo;
+            if (kidx >= 0) kidx += (int)hcnt[b_lo];  // the count above the range shrinks
+          }
+          if (b_hi < kBins - 1 && (!cand_lists || b_hi < bf)) ++b_hi;
+          if (threadIdx.x == 0) sh.bi[4] = 0;
+          __syncthreads();
+        }
         // members of bins [b_lo, b_hi] and the exact mass above them; a logit
         // pre-filter (with margin) skips the E of elements below the range
         const uint32_t edge = (uint32_t)(0x3F7FFFFF - ((b_hi + 1) << 18) + 1);
@@ -1993,12 +2203,23 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
         if (cand_lists) {
           const int cnt = sh.list_n[warp];
-          for (int j = lane; j < cnt; j += 32)
-            consider(lid[warp * WCAP + j], lval[warp * WCAP + j]);
+          for (int j = lane; j < cnt; j += 32) consider(lid[warp * WCAP + j], lval[warp * WCAP + j]);
         } else {
-          sweep([&](int k, float l) {
-            if (l >= lpre) consider(k, l);
-          });
+          // the row, each warp its range, 32 consecutive ids per step, eight
+          // steps' loads in flight
+          for (int k0 = r0; k0 < r1; k0 += 256) {  // warp-uniform
+            float lv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int k = k0 + 32 * u + lane;
+              lv[u] = k < r1 ? ldg_keep(lrow + k, pol) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int k = k0 + 32 * u + lane;
+              if (k < r1 && lv[u] >= lpre) consider(k, lv[u]);
+            }
+          }
         }
         const unsigned long long a_lo = block_sum_u64<NT>(above, sh);  // barriers: members complete
         const int total = sh.bi[4];
@@ -2008,9 +2229,10 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           const int t = threadIdx.x;
           const unsigned long long key = t < total ? xkey[t] : 0ull;
           const uint32_t eb = t < total ? xbits[t] : 0u;
-          if (!select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
-                              zfx, xkey, xbits, &cut, &zkept, sh))
-            tmode = 2;
+          if (select_cut<NT>(key, eb, total, a_lo, kidx, topp, p.top_p,
+                             zfx, xkey, xbits, &cut, &zkept, sh))
+            break;
+          if (attempt == 1) tmode = 2;
         }
       }
       if (tmode == 2) {
@@ -2018,13 +2240,19 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         cut = cut_radix<NT>(p, lrow, [&](int k) { return Eof(__ldg(lrow + k)); }, V, 0, rs, 0, 1,
                             ph, sh);
         float s = 0.f, cmp = 0.f;
-        for (int k = threadIdx.x; k < V; k += NT) {
-          const float l = __ldg(lrow + k);
-          if (is_kept(okey(l), k, cut.tau, cut.tie)) {
-            const float y = Eof(l) - cmp;
-            const float tt = s + y;
-            cmp = (tt - s) - y;
-            s = tt;
+        for (int k0 = threadIdx.x; k0 < V; k0 += 8 * NT) {
+          float lv[8];  // eight logits in flight per thread
+#pragma unroll
+          for (int u = 0; u < 8; ++u) lv[u] = k0 + u * NT < V ? __ldg(lrow + k0 + u * NT) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int k = k0 + u * NT;
+            if (k < V && is_kept(okey(lv[u]), k, cut.tau, cut.tie)) {
+              const float y = Eof(lv[u]) - cmp;
+              const float tt = s + y;
+              cmp = (tt - s) - y;
+              s = tt;
+            }
           }
         }
         const float hs = block_sum_f<NT>(s, sh);
@@ -2118,14 +2346,30 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       __syncthreads();
       const int cnt = min(sh.list_n[warp], WCAP);
       float acc = 0.f;
-      for (int j = lane; j < cnt; j += 32) {
-        float v = lval[warp * WCAP + j];
-        if (mode == 1) {
-          const float qv = v > 0.f ? __ldg(qrow + lid[warp * WCAP + j]) : 0.f;
-          v = residual_w(v, invw, qv);
-          lval[warp * WCAP + j] = v;
+      for (int j0 = 0; j0 < cnt; j0 += 256) {  // eight q loads in flight per lane
+        float vv[8], qq[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + 32 * u + lane;
+          vv[u] = j < cnt ? lval[warp * WCAP + j] : 0.f;
         }
-        acc += v;
+        if (mode == 1) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            qq[u] = (j < cnt && vv[u] > 0.f) ? __ldg(qrow + lid[warp * WCAP + j]) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            if (j < cnt) {
+              vv[u] = residual_w(vv[u], invw, qq[u]);
+              lval[warp * WCAP + j] = vv[u];
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += vv[u];  // ascending j, as one lane's stride
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
@@ -2333,6 +2577,301 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   finish_row(p, row, oc, sh);
 }
 
+// ---------------------------------------------------------------- streaming pre-pass (many rows)
+// Pass 1 of the two-pass streaming sampler, in two kernels.
+//  * sampler_floor_kernel: each row's candidate floor, from 1024 evenly
+//    spaced samples: the deepest bin (32 per octave of E relative to the
+//    samples' maximum) whose sample count at or above it stays within the
+//    list budget, taken as a logit.
+//  * sampler_sweep_kernel: every row swept from HBM once, by one CTA per
+//    warp range of the row kernel (32 per row: the sweep spreads evenly over
+//    every SM, eight CTAs resident per SM).  The CTA copies its whole range
+//    into shared memory at once (16-byte cp.async: about 150 KB in flight per
+//    SM), then in one pass computes the range's maximum, Z relative to the
+//    row samples' maximum (rescaled to the range's), and the ballots of the
+//    ids at or above the floor, from which it writes their list (ascending,
+//    with their logits).
+// The row kernel (pass 2) starts from these results.  Both launches after
+// the first are programmatic dependents: they start while the previous one
+// finishes and wait for its results (griddepcontrol.wait) only where they
+// need them.
+constexpr int kSwMaxPieces = 64;  // 128-id pieces per range (ranges of up to 8192 ids)
+constexpr int kSwCTAs = 5;        // pre-pass CTAs per SM (two range buffers each)
+
+// L2 policy for data read once (the logits in the pre-pass)
+SPEC_DEV uint64_t l2_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// The row's candidate floor as a logit (+inf: no lists).  Every thread
+// returns the same value; contains barriers (call from uniform control flow).
+template <bool FAST>
+SPEC_DEV float row_floor(const SP& p, const float* lrow, uint64_t pol, uint32_t* scnt,
+                         float* sred, int* sbf, float* smax_out) {
+  const int V = p.V, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool topk = p.top_k > 0 && p.top_k < V;
+  const bool topp = p.top_p > 0.f && p.top_p < 1.f;
+  const float budget =
+      topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
+  const int ns = (int)(budget * (float)kSamples / (float)V);
+  const bool want = (topk || topp) && V <= kSListMaxV && ns >= 1 &&
+                    (!topk || p.top_k <= kSBudget / 2);
+  constexpr int SPT = kSamples / kSwNT;  // samples per thread
+  float smp[SPT];
+  float sm = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < SPT; ++u) {
+    const long long j = threadIdx.x + kSwNT * u;
+    smp[u] = ldg_keep(lrow + (int)((j * V) / kSamples), pol);
+    sm = fmax_nan(sm, smp[u]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sm = fmax_nan(sm, __shfl_xor_sync(kFull, sm, o));
+  if (lane == 0) sred[warp] = sm;
+  for (int k = threadIdx.x; k < kHist; k += kSwNT) scnt[k] = 0u;
+  __syncthreads();
+  float smax = sred[0];
+  for (int w = 1; w < kSwW; ++w) smax = fmax_nan(smax, sred[w]);
+  *smax_out = smax;
+  if (!want || !(fabsf(smax) < INFINITY)) return INFINITY;  // uniform
+  const float nm = -smax, lfl = smax - 150.f * p.T, nmc = -smax * p.c_hi;
+#pragma unroll
+  for (int u = 0; u < SPT; ++u) {
+    const float e = FAST ? fexp(smp[u], p.c_hi, nmc) : texp(smp[u], nm, lfl, p.c_hi, p.c_lo);
+    atomicAdd(&scnt[ebin(__float_as_uint(e))], 1u);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // the deepest bin b whose samples in bins <= b number at most ns
+    uint32_t c = 0;
+    for (int b = 32 * lane; b < 32 * lane + 32; ++b) c += scnt[b];
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned h = __ballot_sync(kFull, incl > (uint32_t)ns);
+    int bfs = kBins - 1;
+    if (h) {
+      const int L = __ffs(h) - 1;
+      uint32_t run = __shfl_sync(kFull, incl - c, L);
+      bfs = 32 * L + 31;
+      for (int b = 32 * L; b < 32 * L + 32; ++b) {
+        run += scnt[b];
+        if (run > (uint32_t)ns) {
+          bfs = b - 1;
+          break;
+        }
+      }
+    }
+    if (lane == 0) *sbf = bfs;
+  }
+  __syncthreads();
+  const int bfs = *sbf;
+  if (bfs < 0) return INFINITY;
+  // E >= 2^-(bfs + 1)/32 relative to smax  <=>  l >= smax - (bfs + 1) T ln2 / 32
+  return smax - (float)(bfs + 1) * (p.T * kLn2 * (1.f / 32.f));
+}
+
+template <bool FAST>
+__global__ void __launch_bounds__(kSwNT) sampler_floor_kernel(const SP p) {
+  __shared__ uint32_t scnt[kHist];
+  __shared__ float sred[kSwW];
+  __shared__ int sbf;
+  // the sweep may start now: it waits for this kernel before reading the floors
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int row = blockIdx.x;
+  float smax;
+  const float Lf = row_floor<FAST>(p, p.logits + (size_t)row * p.V, l2_first_policy(), scnt,
+                                   sred, &sbf, &smax);
+  if (threadIdx.x == 0) {
+    p.lfloor[2 * row] = Lf;
+    p.lfloor[2 * row + 1] = smax;
+  }
+}
+
+// One warp range (item = row * 32 + range) whose logits are in buf: its
+// maximum, Z and list.  Warp k takes a contiguous run of 128-id pieces (lane
+// l reads ids 32 j + l of a piece, so ballot j is 32 consecutive ids in
+// order) and appends the flagged ids of its run, ascending, to its own
+// segment of the range's list (kSegCap entries; more marks the range as
+// overflowing).  Every thread calls it; it ends with a barrier, after which
+// buf and the shared arrays may be reused.
+template <bool FAST>
+SPEC_DEV void sweep_range(const SP& p, int item, float* buf, float* wmax, float* wzh, float* wzl,
+                          int* wcnt, uint16_t* stage) {
+  const int row = item / kRangesPerRow, w = item % kRangesPerRow;
+  const int V = p.V, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rw = stream_range_width(V);
+  const int r0 = min(w * rw, V), r1 = min((w + 1) * rw, V);
+  const int n = r1 - r0, npc = (n + 127) / 128;  // ids, 128-id pieces
+  for (int k = n + t; k < 128 * npc; k += kSwNT) buf[k] = -INFINITY;  // the pad
+  const float Lf = p.lfloor[2 * row], sref = p.lfloor[2 * row + 1];
+  const float c_hi = p.c_hi, c_lo = p.c_lo, T150 = 150.f * p.T;
+  __syncthreads();
+  // one pass: the maximum, Z relative to the samples' maximum sref (rescaled
+  // to the range's maximum below), and the flagged ids
+  const unsigned lt = (1u << lane) - 1u;
+  const int ppw = (npc + kSwW - 1) / kSwW;
+  const int q0 = min(warp * ppw, npc), q1 = min(q0 + ppw, npc);
+  uint16_t* wst = stage + warp * kSegCap;  // this warp's staged offsets (within the range)
+  float mx = -INFINITY, zs = 0.f, zc = 0.f;
+  int run = 0;  // warp-uniform: ids appended to this warp's segment
+  {
+    const float nm = -sref, lfl = sref - T150, nmc = -sref * c_hi;
+    for (int q = q0; q < q1; ++q) {
+      float l[4], e[4];
+      uint32_t bal[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        l[j] = buf[128 * q + 32 * j + lane];
+        mx = fmax_nan(mx, l[j]);
+        e[j] = FAST ? fexp(l[j], c_hi, nmc) : texp(l[j], nm, lfl, c_hi, c_lo);
+        bal[j] = __ballot_sync(kFull, l[j] >= Lf);
+      }
+      const float y = ((e[0] + e[1]) + (e[2] + e[3])) - zc;  // Kahan
+      const float tt = zs + y;
+      zc = (tt - zs) - y;
+      zs = tt;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int pos = run + __popc(bal[j] & lt);
+        if (((bal[j] >> lane) & 1u) && pos < kSegCap) wst[pos] = (uint16_t)(128 * q + 32 * j + lane);
+        run += __popc(bal[j]);
+      }
+    }
+  }
+  __syncwarp();  // the warp's staged offsets are written
+  {  // its segment, coalesced: ids and their logits
+    int32_t* oid = p.lid_g + ((size_t)item * kSwW + warp) * kSegCap;
+    float* oval = p.lval_g + ((size_t)item * kSwW + warp) * kSegCap;
+    for (int e = lane; e < min(run, kSegCap); e += 32) {
+      const int off = wst[e];
+      oid[e] = r0 + off;
+      oval[e] = buf[off];
+    }
+  }
+  float zh = zs, zl = -zc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
+    zh += __shfl_xor_sync(kFull, zh, o);
+    zl += __shfl_xor_sync(kFull, zl, o);
+  }
+  if (lane == 0) {
+    wmax[warp] = mx;
+    wzh[warp] = zh;
+    wzl[warp] = zl;
+    wcnt[warp] = run;
+    p.segcnt[(size_t)item * kSwW + warp] = run;
+  }
+  __syncthreads();
+  float M = wmax[0], Zh = wzh[0], Zl = wzl[0];
+  int total = 0;
+  bool over = false;
+  for (int i = 0; i < kSwW; ++i) {
+    if (i > 0) {
+      M = fmax_nan(M, wmax[i]);
+      Zh += wzh[i];
+      Zl += wzl[i];
+    }
+    total += wcnt[i];
+    over |= wcnt[i] > kSegCap;
+  }
+  RangeStat res{M, 0.f, 0.f, over ? kSWCap + 1 : total};
+  if (fabsf(M) < INFINITY) {  // uniform; else Z is not needed
+    if (fabsf(Zh) < INFINITY) {
+      // Z relative to M: times E(sref) relative to M, the product's error kept in the pair
+      const float sc = FAST ? fexp(sref, c_hi, -M * c_hi) : texp(sref, -M, M - T150, c_hi, c_lo);
+      const float h = Zh * sc;
+      res.zh = h;
+      res.zl = __fmaf_rn(Zh, sc, -h) + Zl * sc;
+    } else {
+      // E relative to sref overflowed (a range far above the samples): Z again
+      // relative to M, from the logits still in shared memory
+      const float nm = -M, lfl = M - T150, nmc = -M * c_hi;
+      float s2 = 0.f, c2 = 0.f;
+      for (int k = t; k < 128 * npc; k += kSwNT) {
+        const float e = FAST ? fexp(buf[k], c_hi, nmc) : texp(buf[k], nm, lfl, c_hi, c_lo);
+        const float y = e - c2, tt = s2 + y;
+        c2 = (tt - s2) - y;
+        s2 = tt;
+      }
+      float h = s2, lo = -c2;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        h += __shfl_xor_sync(kFull, h, o);
+        lo += __shfl_xor_sync(kFull, lo, o);
+      }
+      __syncthreads();  // every thread has read wzh / wzl above
+      if (lane == 0) {
+        wzh[warp] = h;
+        wzl[warp] = lo;
+      }
+      __syncthreads();
+      for (int i = 0; i < kSwW; ++i) {
+        res.zh += wzh[i];
+        res.zl += wzl[i];
+      }
+    }
+  } else {
+    res.cnt = 0;
+  }
+  if (t == 0) p.stats[item] = res;
+  __syncthreads();
+}
+
+// Persistent: each CTA loops over items blockIdx.x, + gridDim.x, ...; the
+// next item's logits are copied into the second buffer (16-byte cp.async,
+// L2 -> shared) while the current one is processed.  Rows that are not
+// 16-byte aligned (V % 4 != 0) are loaded with plain loads instead.
+template <bool FAST>
+__global__ void __launch_bounds__(kSwNT, kSwCTAs) sampler_sweep_kernel(const SP p) {
+  extern __shared__ __align__(16) uint8_t dyn[];  // two buffers of `cap` floats
+  __shared__ float wmax[kSwW], wzh[kSwW], wzl[kSwW];
+  __shared__ int wcnt[kSwW];
+  __shared__ uint16_t stage[kSwW * kSegCap];  // flagged offsets staged per warp
+  const int V = p.V, t = threadIdx.x;
+  const int rw = stream_range_width(V);
+  const int cap = (rw + 127) / 128 * 128;
+  const int items = p.B * p.R * kRangesPerRow;
+  const uint64_t pol = l2_first_policy();
+  float* bufs = reinterpret_cast<float*>(dyn);
+  auto issue = [&](int item, float* buf) {
+    const int row = item / kRangesPerRow, w = item % kRangesPerRow;
+    const int r0 = min(w * rw, V), n = min((w + 1) * rw, V) - r0;
+    const float* src = p.logits + (size_t)row * V + r0;
+    if (p.bulk != 0) {  // V % 4 == 0: r0 and n are multiples of 4
+      const uint32_t sbuf = smem_u32(buf);
+      for (int q = t; q < n / 4; q += kSwNT)
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                         sbuf + 16 * q),
+                     "l"(src + 4 * q), "l"(pol)
+                     : "memory");
+    } else {
+      for (int k = t; k < n; k += kSwNT) buf[k] = ldg_keep(src + k, pol);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  int item = blockIdx.x;
+  if (item < items) issue(item, bufs);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the floors are written
+  for (int k = 0; item < items; ++k, item += gridDim.x) {
+    const int nxt = item + gridDim.x;
+    if (nxt < items) {
+      issue(nxt, bufs + ((k + 1) & 1) * cap);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this item's copies have landed
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    sweep_range<FAST>(p, item, bufs + (k & 1) * cap, wmax, wzh, wzl, wcnt, stage);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- host side
 struct SampPlan {
   int CS, slice, NT;
@@ -2373,13 +2912,42 @@ SampPlan plan_sampler(int B, int R, int V, bool qsm) {
   return pl;
 }
 
-size_t samp_ws(int B, int R, size_t* off_out, size_t* off_cnt) {
+// Workspace: header, row outcomes, sequence counters; with `pre`, the
+// streaming pre-pass results after them (see SP).
+struct SampWs {
+  size_t out, cnt, stats, lfloor, lid, lval, segcnt, end;
+};
+
+SampWs samp_ws(int B, int R, bool pre) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = (size_t)B * R;
+  SampWs w;
   size_t off = sizeof(WsHeader);
-  *off_out = off;
-  off += ((size_t)B * R * sizeof(Outcome) + 255) / 256 * 256;
-  *off_cnt = off;
-  off += ((size_t)B * sizeof(int32_t) + 255) / 256 * 256;
-  return off;
+  w.out = off;
+  off += up(rows * sizeof(Outcome));
+  w.cnt = off;
+  off += up((size_t)B * sizeof(int32_t));
+  w.stats = w.lfloor = w.lid = w.lval = w.segcnt = 0;
+  if (pre) {
+    w.stats = off;
+    off += up(rows * kRangesPerRow * sizeof(RangeStat));
+    w.lfloor = off;
+    off += up(rows * 2 * sizeof(float));
+    const size_t seg = rows * kRangesPerRow * kSwW;
+    w.lid = off;
+    off += up(seg * kSegCap * sizeof(int32_t));
+    w.lval = off;
+    off += up(seg * kSegCap * sizeof(float));
+    w.segcnt = off;
+    off += up(seg * sizeof(int32_t));
+  }
+  w.end = off;
+  return w;
+}
+
+// many rows: the streaming kernels (with truncated sampling) rather than clusters
+bool many_rows(int B, int R, int V) {
+  return (long long)B * R * cluster_size(V) > 2LL * num_sms_cached();
 }
 
 template <int NT, bool FAST, bool TR>
@@ -2410,40 +2978,88 @@ size_t stream_smem(int V) {
   return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8 + words * 4;
 }
 
-template <bool FAST>
+// the row kernel, after the pre-pass when PRE (a programmatic dependent: its
+// CTAs start as the pre-pass's last ones finish and wait for its results)
+template <bool FAST, bool PRE>
 spec_status launch_stream(const SP& prm, int rows, cudaStream_t st) {
   static PerDeviceOnce<int> smem_once;  // once per device, at the largest size
-  const spec_status ra = ensure_smem_limit(smem_once, (const void*)sampler_stream_kernel<FAST>,
+  const spec_status ra = ensure_smem_limit(smem_once, (const void*)sampler_stream_kernel<FAST, PRE>,
                                            (int)stream_smem(kSListMaxV));
   if (ra != SPEC_OK) return ra;
+  if (PRE) {
+    constexpr int kSwSmemMax = 2 * kSwMaxPieces * 128 * (int)sizeof(float);
+    const int sw_smem = 2 * ((stream_range_width(prm.V) + 127) / 128 * 128) * (int)sizeof(float);
+    if (sw_smem > kSwSmemMax) return SPEC_EUNSUPPORTED;
+    static PerDeviceOnce<int> sw_once;  // once per device, at the largest size
+    const spec_status rb =
+        ensure_smem_limit(sw_once, (const void*)sampler_sweep_kernel<FAST>, kSwSmemMax);
+    if (rb != SPEC_OK) return rb;
+    sampler_floor_kernel<FAST><<<(unsigned)rows, kSwNT, 0, st>>>(prm);
+    spec_status rs = launch_status();
+    if (rs != SPEC_OK) return rs;
+    cudaLaunchConfig_t c1 = {};
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sampler_sweep_kernel<FAST>, kSwNT,
+                                                      (size_t)sw_smem) != cudaSuccess ||
+        per_sm < 1)
+      return SPEC_ECUDA;
+    const long long items = (long long)rows * kRangesPerRow;
+    c1.gridDim = dim3((unsigned)std::min<long long>(items, (long long)per_sm * num_sms_cached()),
+                      1, 1);
+    c1.blockDim = dim3(kSwNT, 1, 1);
+    c1.dynamicSmemBytes = (size_t)sw_smem;
+    c1.stream = st;
+    cudaLaunchAttribute a1[1];
+    a1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a1[0].val.programmaticStreamSerializationAllowed = 1;
+    c1.attrs = a1;
+    c1.numAttrs = 1;
+    if (cudaLaunchKernelEx(&c1, sampler_sweep_kernel<FAST>, prm) != cudaSuccess) return SPEC_ECUDA;
+    rs = launch_status();
+    if (rs != SPEC_OK) return rs;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows, 1, 1);
   cfg.blockDim = dim3(kSNT, 1, 1);
   cfg.dynamicSmemBytes = stream_smem(prm.V);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (its radix fallback
   attr[0].val.clusterDim.x = 1;                        // uses the cluster exchange helpers)
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sampler_stream_kernel<FAST>, prm) != cudaSuccess) return SPEC_ECUDA;
+  cfg.numAttrs = PRE ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, sampler_stream_kernel<FAST, PRE>, prm) != cudaSuccess)
+    return SPEC_ECUDA;
   return launch_status();
 }
 
-spec_status launch_sampler(SP prm, int B, int R, int V, cudaStream_t st) {
+spec_status launch_sampler(SP prm, int B, int R, int V, size_t ws_bytes, cudaStream_t st) {
   // full-vocabulary residuals (no truncation) stage q's slice in shared memory
   const bool trunc = (prm.top_k > 0 && prm.top_k < V) || (prm.top_p > 0.f && prm.top_p < 1.f);
   // many truncated rows: one streaming CTA per row (every SM busy, no
   // cluster exchanges); trees only when their kept set fits the lists
   {
-    const long long ctas = (long long)B * R * cluster_size(V);
-    const bool many = ctas > 2LL * num_sms_cached();
-    if (many && trunc && !prm.greedy &&
+    if (many_rows(B, R, V) && trunc && !prm.greedy &&
         (!prm.tree || (prm.top_k > 0 && prm.top_k <= kSCap / (kSNT / 32)))) {
       prm.slice = V;
-      return prm.p_out ? launch_stream<false>(prm, B * R, st) : launch_stream<true>(prm, B * R, st);
+      // two passes when the workspace holds the pre-pass results
+      const SampWs w = samp_ws(B, R, true);
+      if (ws_bytes >= w.end) {
+        uint8_t* base = reinterpret_cast<uint8_t*>(prm.err);
+        prm.stats = reinterpret_cast<RangeStat*>(base + w.stats);
+        prm.lfloor = reinterpret_cast<float*>(base + w.lfloor);
+        prm.lid_g = reinterpret_cast<int32_t*>(base + w.lid);
+        prm.lval_g = reinterpret_cast<float*>(base + w.lval);
+        prm.segcnt = reinterpret_cast<int32_t*>(base + w.segcnt);
+        return prm.p_out ? launch_stream<false, true>(prm, B * R, st)
+                         : launch_stream<true, true>(prm, B * R, st);
+      }
+      return prm.p_out ? launch_stream<false, false>(prm, B * R, st)
+                       : launch_stream<true, false>(prm, B * R, st);
     }
   }
   prm.qsm = (!prm.greedy && prm.qbulk && !trunc) ? 1 : 0;
@@ -2489,12 +3105,11 @@ SP base_params(const float* logits, const float* q, const float* u, int B, int R
   prm.top_p = cfg->top_p;
   prm.greedy = cfg->greedy ? 1 : 0;
   prm.eos = cfg->eos_id;
-  size_t off_out, off_cnt;
-  samp_ws(B, R, &off_out, &off_cnt);
+  const SampWs sw = samp_ws(B, R, false);
   uint8_t* w = static_cast<uint8_t*>(ws);
   prm.err = reinterpret_cast<int32_t*>(w);
-  prm.outcomes = reinterpret_cast<Outcome*>(w + off_out);
-  prm.seq_count = reinterpret_cast<int32_t*>(w + off_cnt);
+  prm.outcomes = reinterpret_cast<Outcome*>(w + sw.out);
+  prm.seq_count = reinterpret_cast<int32_t*>(w + sw.cnt);
   prm.bulk = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) ? 1 : 0;
   prm.qbulk = (q && V % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0) ? 1 : 0;
   return prm;
@@ -2505,10 +3120,13 @@ bool slice_fits(int V) { return (size_t)slice_of(V, cluster_size(V)) * 4 <= kMax
 }  // namespace
 
 extern "C" size_t spec_accept_sample_workspace_size(int B, int R, int V) {
-  (void)V;
-  if (B < 0 || R < 1) return 0;
-  size_t a, c;
-  return samp_ws(B, R, &a, &c);
+  if (B < 0 || R < 1 || V < 1) return 0;
+  return samp_ws(B, R, false).end;
+}
+
+extern "C" size_t spec_accept_sample_workspace_size_two_pass(int B, int R, int V) {
+  if (B < 0 || R < 1 || V < 1) return 0;
+  return samp_ws(B, R, many_rows(B, R, V)).end;
 }
 
 extern "C" spec_status spec_accept_sample(const float* target_logits, const float* draft_probs,
@@ -2526,8 +3144,7 @@ extern "C" spec_status spec_accept_sample(const float* target_logits, const floa
   if (!cfg->greedy && (!uniforms || (R > 1 && !draft_probs))) return SPEC_EINVAL;
   if (R > kMaxN || (long long)B * R * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
   if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
-  size_t a, c;
-  if (workspace_bytes < samp_ws(B, R, &a, &c)) return SPEC_EINVAL;
+  if (workspace_bytes < samp_ws(B, R, false).end) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;
   SP prm = base_params(target_logits, draft_probs, uniforms, B, R, V, cfg, workspace);
   prm.tokens = draft_tokens;
@@ -2536,7 +3153,7 @@ extern "C" spec_status spec_accept_sample(const float* target_logits, const floa
   prm.emitted = emitted;
   prm.p_out = cfg->greedy ? nullptr : p_out;
   prm.status = status_per_seq;
-  return launch_sampler(prm, B, R, V, static_cast<cudaStream_t>(stream));
+  return launch_sampler(prm, B, R, V, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" spec_status spec_accept_sample_tree(const float* target_logits,
@@ -2557,8 +3174,7 @@ extern "C" spec_status spec_accept_sample_tree(const float* target_logits,
   if (!cfg->greedy && (!uniforms || !draft_probs)) return SPEC_EINVAL;
   if (N > kMaxN || (long long)B * N * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
   if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
-  size_t a, c;
-  if (workspace_bytes < samp_ws(B, N, &a, &c)) return SPEC_EINVAL;
+  if (workspace_bytes < samp_ws(B, N, false).end) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;
   SP prm = base_params(target_logits, draft_probs, uniforms, B, N, V, cfg, workspace);
   prm.tokens = node_tokens;
@@ -2569,5 +3185,5 @@ extern "C" spec_status spec_accept_sample_tree(const float* target_logits,
   prm.emitted = emitted;
   prm.p_out = cfg->greedy ? nullptr : p_out;
   prm.status = status_per_seq;
-  return launch_sampler(prm, B, N, V, static_cast<cudaStream_t>(stream));
+  return launch_sampler(prm, B, N, V, workspace_bytes, static_cast<cudaStream_t>(stream));
 }

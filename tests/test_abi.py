@@ -110,6 +110,15 @@ def test_workspace_sizes(lib):
     # explicit splits are honoured up to the 64-token stage granularity
     assert sv.attn_num_splits(1, 16, 64, 8, 128, 16, 8193, 128) >= 128
     assert sv.sample_workspace_size(4, 64, 128256) >= 256 + 4 * 64 * 16
+    # the two-pass variant: few rows need nothing more; many rows room for the
+    # pre-pass results (per row: 32 range records, 32 x 8 segments of 128 listed
+    # ids and logits, their counts, the floor)
+    few, mn = sv.sample_workspace_size(1, 8, 128256, True), sv.sample_workspace_size(1, 8, 128256)
+    assert few == mn and mn % 256 == 0
+    big, mn = sv.sample_workspace_size(64, 5, 152064, True), sv.sample_workspace_size(64, 5, 152064)
+    assert big >= mn + 320 * (32 * 16 + 32 * 8 * 128 * 8 + 32 * 8 * 4 + 8)
+    assert sv.sample_workspace_size(64, 5, 0) == 0          # no vocabulary: invalid
+    assert sv.sample_workspace_size(64, 5, 0, True) == 0
 
 
 def test_kv_commit_host_validation(lib):

@@ -30,17 +30,26 @@ def _api_cfg(c: SamplerCfg) -> sv.SamplerConfig:
                             greedy=c.greedy, eos_id=c.eos_id)
 
 
-def run_chain(logits, q, drafts, u, cfg: SamplerCfg, want_p=True):
+def _ws(B, R, V, two_pass):
+    """The default workspace (one-kernel streaming variant for many rows), or
+    one with room for the two-pass variant, which it selects."""
+    return sv.new_workspace(sv.sample_workspace_size(B, R, V, two_pass=two_pass), DEV)
+
+
+def run_chain(logits, q, drafts, u, cfg: SamplerCfg, want_p=True, two_pass=False):
     t = lambda a: None if a is None else torch.as_tensor(a).to(DEV).contiguous()  # noqa: E731
+    B, R, V = np.shape(logits)
     res = sv.accept_sample(t(logits), t(q), t(drafts), t(u), _api_cfg(cfg),
-                           want_p=want_p and not cfg.greedy)
+                           workspace=_ws(B, R, V, two_pass), want_p=want_p and not cfg.greedy)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def run_tree(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=True):
+def run_tree(logits, q, tokens, parent, u, cfg: SamplerCfg, want_p=True, two_pass=False):
     t = lambda a: None if a is None else torch.as_tensor(a).to(DEV).contiguous()  # noqa: E731
+    B, N, V = np.shape(logits)
     res = sv.accept_sample_tree(t(logits), t(q), t(tokens), t(parent), t(u), _api_cfg(cfg),
+                                workspace=_ws(B, N, V, two_pass),
                                 want_p=want_p and not cfg.greedy)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
@@ -291,9 +300,10 @@ def test_batched_serving_full_size(name):
     w, gpu, ref = chain_case(spec, spec.seed)
     compare(gpu, ref)
     check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
-    gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
-                     want_p=False)
-    compare(gpu2, ref)
+    for two_pass in (False, True):   # one-kernel and two-pass streaming variants
+        gpu2 = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg_of(spec),
+                         want_p=False, two_pass=two_pass)
+        compare(gpu2, ref)
 
 
 STREAM_SHAPES = [
@@ -326,12 +336,45 @@ def test_many_rows_floor_fallbacks(name, kw, sd, clustered, V):
                                             w.draft_tokens.numpy(), w.uniforms.numpy(), cfg,
                                             want_p=True)
     for want_p in (True, False):
-        gpu = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg, want_p)
-        # flat_topp: every token is lighter than the flag margin, so the top-p cutoff is
-        # ambiguous by construction and may flag every sequence
-        compare(gpu, ref, max_flagged=spec.B if name == "flat_topp" else None)
-        if want_p:
-            check_p(gpu["p"], ref, w.logits.numpy(), cfg)
+        for two_pass in (False, True):   # one-kernel and two-pass streaming variants
+            gpu = run_chain(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg, want_p,
+                            two_pass=two_pass)
+            # flat_topp: every token is lighter than the flag margin, so the top-p cutoff is
+            # ambiguous by construction and may flag every sequence
+            compare(gpu, ref, max_flagged=spec.B if name == "flat_topp" else None)
+            if want_p:
+                check_p(gpu["p"], ref, w.logits.numpy(), cfg)
+
+
+def test_many_rows_nonfinite_and_banned():
+    """Many rows: NaN or +inf in a row marks its sequence, a row of -inf but
+    one token keeps only that token, in both streaming variants."""
+    spec = wl.Spec("nonfinite", B=64, Hq=1, Hkv=1, D=64, V=6000, ctx=(1, 1), gamma=4,
+                   logit_sd=3.0, temperature=1.0, top_p=0.9, draft_div=1.0, draft_noise=0.8)
+    w = wl.make_sampler_inputs(spec, seed=21)
+    logits = w.logits.numpy().copy()
+    logits[1, 0, 17] = np.nan
+    logits[2, 0, 4001] = np.inf
+    logits[3, 0, :] = -np.inf
+    logits[3, 0, 77] = 0.0              # only token 77 can be drawn from row 0
+    logits[4, 2, ::3] = -np.inf         # banned tokens in a row that may be read
+    cfg = cfg_of(spec)
+    ok = np.ones(spec.B, bool)
+    ok[[1, 2]] = False
+    ref = oracle.sampler.accept_chain_batch(logits[ok], w.draft_probs.numpy()[ok],
+                                            w.draft_tokens.numpy()[ok], w.uniforms.numpy()[ok],
+                                            cfg, want_p=True)
+    for two_pass in (False, True):
+        for want_p in (True, False):
+            gpu = run_chain(logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg, want_p,
+                            two_pass=two_pass)
+            for b in (1, 2):
+                assert gpu["status"][b] & sv.api.SEQ_NONFINITE and gpu["accepted_len"][b] == -1
+                assert (gpu["emitted"][b] == -1).all()
+            sub = {k: v[ok] for k, v in gpu.items()}
+            compare(sub, ref)
+            if want_p:
+                check_p(sub["p"], ref, logits[ok], cfg)
 
 
 # ------------------------------------------------------------------ tree
@@ -366,9 +409,10 @@ def test_tree_draft_tree_config():
     w, gpu, ref = tree_case(spec, spec.seed)
     compare(gpu, ref, tree=True)
     check_p(gpu["p"], ref, w.logits.numpy(), cfg_of(spec))
-    gpu2 = run_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms, cfg_of(spec),
-                    want_p=False)
-    compare(gpu2, ref, tree=True)
+    for two_pass in (False, True):   # one-kernel and two-pass streaming variants
+        gpu2 = run_tree(w.logits, w.draft_probs, w.draft_tokens, w.parent, w.uniforms,
+                        cfg_of(spec), want_p=False, two_pass=two_pass)
+        compare(gpu2, ref, tree=True)
 
 
 def test_tree_first_token_follows_p_root_on_gpu():
