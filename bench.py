@@ -322,10 +322,20 @@ def time_step(step: GpuStep, steps: int, warmup: int, flush_l2, ws: int, gpu_ind
             e1.record(stream)
             e1.synchronize()
             part_ms.append(e0.elapsed_time(e1))
+    # the partial pass alone (nothing running beside it), right after the timed
+    # region: inside the step the sampler's CTAs share its SMs and stretch it
+    iso_ms = []
+    for _ in range(min(steps, 50)):
+        flush_l2()
+        e0.record(stream)
+        step.attn.partials()
+        e1.record(stream)
+        e1.synchronize()
+        iso_ms.append(e0.elapsed_time(e1))
     err = step.sv.workspace_error(step.attn.workspace) | step.sv.workspace_error(step.sws)
     if err:
         raise RuntimeError(f"device wait timed out (error word {err:#x})")
-    return {"step_ms": step_ms, "part_ms": part_ms, "samp_ms": samp_ms,
+    return {"step_ms": step_ms, "part_ms": part_ms, "samp_ms": samp_ms, "iso_part_ms": iso_ms,
             "clocks": clk.summary() if clk else None}
 
 
@@ -361,6 +371,8 @@ def step_record(spec, step, t, nbytes, peak, ws, dev):
         "step_hbm_frac_all_q_rows": nbytes["step_all_q"] / (med * 1e-3) / 1e9 / peak,
         "attn_partial_us": part * 1e3,
         "attn_partial_frac": nbytes["attn"] / (part * 1e-3) / 1e9 / peak,
+        "attn_partial_alone_us": (statistics.median(t["iso_part_ms"]) * 1e3
+                                  if t.get("iso_part_ms") else None),
         "sampler_us": statistics.fmean(t["samp_ms"]) * 1e3 if t["samp_ms"] else None,
         "attn_num_splits": step.sv.attn_num_splits(
             spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
@@ -373,6 +385,9 @@ def step_record(spec, step, t, nbytes, peak, ws, dev):
         tpk, _ = bf16_peak()
         rec["attn_partial_tflops"] = flop / (part * 1e-3) / 1e12
         rec["attn_partial_tensor_frac"] = rec["attn_partial_tflops"] / tpk
+        if rec["attn_partial_alone_us"]:
+            rec["attn_partial_alone_tflops"] = flop / (rec["attn_partial_alone_us"] * 1e-6) / 1e12
+            rec["attn_partial_alone_tensor_frac"] = rec["attn_partial_alone_tflops"] / tpk
     return rec
 
 
@@ -412,7 +427,8 @@ def bench_gpu(args, spec, ws, rank, local):
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": nbytes["attn"], "mean_launch_us": part_mean * 1e6,
-                     "peak_source": peak_src},
+                     "peak_source": peak_src,
+                     "alone": alone_roofline(t["iso_part_ms"], nbytes["attn"], peak)},
         **acceptance_stats(spec, acc),
         "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps,
@@ -423,6 +439,17 @@ def bench_gpu(args, spec, ws, rank, local):
         torch.cuda.empty_cache()
         out["per_workload"] = per_workload(args, spec, ws, dev, flush_l2, peak)
     return out
+
+
+def alone_roofline(iso_ms, nbytes, peak):
+    """The partial pass timed alone (L2 flushed, CUDA events), after the timed
+    region: its rate without the sampler's CTAs on the same SMs."""
+    if not iso_ms:
+        return None
+    us = statistics.median(iso_ms) * 1e3
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"median_launch_us": us, "achieved": gbs, "frac": gbs / peak,
+            "launches": len(iso_ms)}
 
 
 def partial_kernel_name(spec) -> str:

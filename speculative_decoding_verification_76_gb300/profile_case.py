@@ -21,7 +21,8 @@ def main(argv):
     spec = wl.SPECS[name].with_(B=B)
     if what == "attn":
         w = wl.make_attention_inputs(spec, device="cuda")
-        anc, _, _ = sv.tree_prepare(w.parent, w.ctx_len)
+        # a chain needs no mask (the causal block), as in the verify step
+        anc = sv.tree_prepare(w.parent, w.ctx_len)[0] if spec.is_tree else None
         call = sv.AttnCall(w.q, w.k_cache, w.v_cache, w.block_table, w.ctx_len, anc,
                            num_splits=spec.num_splits)
         for _ in range(reps):
