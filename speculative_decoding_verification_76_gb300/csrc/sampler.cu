@@ -1815,29 +1815,113 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   };
   const unsigned lt = (1u << lane) - 1u;
 
-  // ---- 1. maximum (NaN-propagating); one sample per thread, evenly spaced
-  // over the row, for the candidate floor.  PRE: every warp combines the
-  // ranges' maxima (lane r holds range r's results)
-  const float smp =
-      (!PRE && trunc) ? ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol) : 0.f;
+  // ---- 1. the maximum (NaN-propagating) and Z.  PRE: every warp combines
+  // the ranges' maxima (lane r holds range r's results).  Otherwise one sweep
+  // of the row: one sample per thread, evenly spaced, gives a reference
+  // maximum sref and the candidate floor Lf (a logit); the sweep then takes
+  // the maximum, Z relative to sref (rescaled to the maximum after it) and a
+  // bit per id at or above Lf
   float m;
   RangeStat st{0.f, 0.f, 0.f, 0};
+  float Lf = INFINITY;              // candidate floor (+inf: no lists)
+  float zh_sw = 0.f, zl_sw = 0.f;   // Z of the sweep (relative to m), float pair
+  const float c_hi = p.c_hi, c_lo = p.c_lo, T150 = 150.f * p.T;
   if constexpr (PRE) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the pre-pass has completed
     st = p.stats[(size_t)row * kRangesPerRow + lane];
     m = st.m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
+    Lf = p.lfloor[2 * row];
   } else {
-    float mx = -INFINITY;
-    sweep([&](int, float l) { mx = fmax_nan(mx, l); });
+    const float smp = ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol);
+    float sm = smp;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm = fmax_nan(sm, __shfl_xor_sync(kFull, sm, o));
+    if (lane == 0) sh.red_f[warp] = sm;
+    __syncthreads();
+    float sref = sh.red_f[0];
+    for (int w = 1; w < NW; ++w) sref = fmax_nan(sref, sh.red_f[w]);
+    const bool sref_ok = fabsf(sref) < INFINITY;  // uniform
+    const float snmc = -sref * c_hi, snm = -sref, slfl = sref - T150;
+    auto Eref = [&](float l) {
+      return FAST ? fexp(l, c_hi, snmc) : texp(l, snm, slfl, c_hi, c_lo);
+    };
+    if (trunc && V <= kSListMaxV && sref_ok) {
+      // the deepest bin of E relative to sref (32 per octave) whose sampled
+      // count at or above it stays within the list budget, taken as a logit
+      const float budget =
+          topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
+      const int ns = (int)(budget * (float)NT / (float)V);
+      if (ns >= 1 && (!topk || p.top_k <= kSBudget / 2)) {
+        const int sbin = ebin(__float_as_uint(Eref(smp)));
+        int lo = -1, hi = kBins - 1;  // the largest b with count(sample bin <= b) <= ns
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (__syncthreads_count(sbin <= mid) <= ns) lo = mid; else hi = mid - 1;
+        }
+        if (lo >= 0) Lf = sref - (float)(lo + 1) * (p.T * kLn2 * (1.f / 32.f));
+      }
+    }
+    const bool flagging = Lf < INFINITY;
+    float mx = -INFINITY, zs = 0.f, zc = 0.f;
+    for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
+      float lv[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load4(s0 + 128 * u + 4 * lane, lv[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = s0 + 128 * u + 4 * lane;
+        float e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mx = fmax_nan(mx, lv[u][j]);
+          e[j] = Eref(lv[u][j]);  // 0 past the range
+        }
+        const float y = ((e[0] + e[1]) + (e[2] + e[3])) - zc;  // Kahan
+        const float t = zs + y;
+        zc = (t - zs) - y;
+        zs = t;
+        if (flagging) {  // a word of 32 consecutive ids per eight lanes
+          uint32_t nib = (lv[u][0] >= Lf ? 1u : 0u) | (lv[u][1] >= Lf ? 2u : 0u) |
+                         (lv[u][2] >= Lf ? 4u : 0u) | (lv[u][3] >= Lf ? 8u : 0u);
+          nib <<= 4 * (lane & 7);
+          nib |= __shfl_xor_sync(kFull, nib, 1);
+          nib |= __shfl_xor_sync(kFull, nib, 2);
+          nib |= __shfl_xor_sync(kFull, nib, 4);
+          if ((lane & 7) == 0 && k < r1) fbits[k >> 5] = nib;
+        }
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(kFull, mx, o));
+    __syncthreads();  // every thread has read sh.red_f above
     if (lane == 0) sh.red_f[warp] = mx;
     __syncthreads();
     m = sh.red_f[0];
     for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.red_f[w]);
-    __syncthreads();
+    __syncthreads();  // every thread has m before the sums reuse sh.red_f
+    const float Zh = block_sum_f<NT>(zs, sh), Zl = block_sum_f<NT>(-zc, sh);
+    if (fabsf(m) < INFINITY) {  // uniform
+      if (sref_ok && fabsf(Zh) < INFINITY) {
+        // relative to m: times E(sref) relative to m, the product's error in the pair
+        const float sc = FAST ? fexp(sref, c_hi, -m * c_hi) : texp(sref, -m, m - T150, c_hi, c_lo);
+        zh_sw = Zh * sc;
+        zl_sw = __fmaf_rn(Zh, sc, -zh_sw) + Zl * sc;
+      } else {
+        // E relative to sref overflowed (or no reference): Z again relative to m
+        const float nm2 = -m, lfl2 = m - T150, nmc2 = -m * c_hi;
+        float s2 = 0.f, c2 = 0.f;
+        sweep([&](int, float l) {
+          const float y = (FAST ? fexp(l, c_hi, nmc2) : texp(l, nm2, lfl2, c_hi, c_lo)) - c2;
+          const float t = s2 + y;
+          c2 = (t - s2) - y;
+          s2 = t;
+        });
+        zh_sw = block_sum_f<NT>(s2, sh);
+        zl_sw = block_sum_f<NT>(-c2, sh);
+      }
+    }
   }
   const bool bad = isnan(m) || m == INFINITY || m == -INFINITY;
   Outcome oc{0, -1, 0, bad ? 1 : 0};
@@ -1851,7 +1935,6 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 
   if (!bad) {
     const float nm = -m, lfloor = m - 150.f * p.T;
-    const float c_hi = p.c_hi, c_lo = p.c_lo;
     const float nmc = -m * c_hi;
     auto Eof = [&](float l) { return FAST ? fexp(l, c_hi, nmc) : texp(l, nm, lfloor, c_hi, c_lo); };
     auto hist = [&](uint32_t bits, int bn) {
@@ -1863,46 +1946,14 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       hist(bits, ebin(bits));
     };
 
-    // ---- 2. the candidate floor (truncated rows): the deepest E bin whose
-    // sampled count at or above it stays within the list budget; the elements
-    // of bins <= bf are listed.  -1: no floor (every element histogrammed)
+    // ---- 2. the listed bins: those whose every element lies at or above the
+    // floor Lf, i.e. above the bin of E at Lf (taken 2^-12 high, which covers
+    // the rounding of E); -1: no lists (every element histogrammed)
     int bf = -1;
-    if constexpr (PRE) {
-      // the bins whose every element lies at or above the pre-pass's floor:
-      // those above the bin of E at the floor (taken 2^-12 high, which covers
-      // the rounding of E)
-      const float Lf = p.lfloor[2 * row];
-      if (trunc && Lf < INFINITY) bf = ebin(__float_as_uint(Eof(Lf) * 1.000244140625f)) - 1;
-    } else if (trunc && V <= kSListMaxV) {
-      const float budget =
-          topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
-      const int ns = (int)(budget * (float)NT / (float)V);
-      if (ns >= 1 && (!topk || p.top_k <= kSBudget / 2)) {
-        const int sbin = ebin(__float_as_uint(Eof(smp)));
-        int lo = -1, hi = kBins - 1;  // the largest b with count(sample bin <= b) <= ns
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (__syncthreads_count(sbin <= mid) <= ns) lo = mid; else hi = mid - 1;
-        }
-        bf = lo;
-      }
-    }
+    if (trunc && Lf < INFINITY) bf = ebin(__float_as_uint(Eof(Lf) * 1.000244140625f)) - 1;
     const bool listing = bf >= 0;
-    // E bits at or above edge_f <=> bin <= bf
-    const uint32_t edge_f = listing ? (uint32_t)(0x3F7FFFFF - ((bf + 1) << 18) + 1) : 0xFFFFFFFFu;
 
-    // ---- 3. Z (E recomputed, compensated per thread), each warp over its own
-    // range; with a floor, one bit per id for the elements at or above it (a
-    // word of 32 consecutive ids per eight lanes), else the histogram of every
-    // element
-    const bool zhist = trunc && !listing;
-    float zs = 0.f, zc = 0.f;
-    auto kahan = [&](float x) {
-      const float y = x - zc;
-      const float t = zs + y;
-      zc = (t - zs) - y;
-      zs = t;
-    };
+    // ---- 3. (PRE) Z: the ranges' Z combined
     if constexpr (PRE) {
       if (warp == 0) {
         // Z = sum over the ranges of Z_r E(m_r), in float pairs, fixed order
@@ -1920,41 +1971,12 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           sh.zpre[1] = zl2;
         }
       }
-    } else
-    for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
-      float lv[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) load4(s0 + 128 * u + 4 * lane, lv[u]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = s0 + 128 * u + 4 * lane;
-        float e[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) e[j] = Eof(lv[u][j]);  // 0 past the range
-        kahan((e[0] + e[1]) + (e[2] + e[3]));
-        if (zhist) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (k + j < r1) hist_e(e[j]);
-        }
-        if (listing) {
-          uint32_t nib = (__float_as_uint(e[0]) >= edge_f ? 1u : 0u) |
-                         (__float_as_uint(e[1]) >= edge_f ? 2u : 0u) |
-                         (__float_as_uint(e[2]) >= edge_f ? 4u : 0u) |
-                         (__float_as_uint(e[3]) >= edge_f ? 8u : 0u);
-          nib <<= 4 * (lane & 7);
-          nib |= __shfl_xor_sync(kFull, nib, 1);
-          nib |= __shfl_xor_sync(kFull, nib, 2);
-          nib |= __shfl_xor_sync(kFull, nib, 4);
-          if ((lane & 7) == 0 && k < r1) fbits[k >> 5] = nib;
-        }
-      }
     }
     if (threadIdx.x == 0 && probe >= 0 && probe < V) sh.eprobe = Eof(l_probe);
 
     // ---- 4. the candidate lists: each warp lists the flagged ids of its
     // range in id order, then loads their logits; the histogram of the listed
-    // elements (exactly those of bins <= bf); if a list overflowed, of every
+    // elements of bins <= bf; without lists, or if a list overflowed, of every
     // element
     int cntw = 0;
     if (PRE) {
@@ -2043,7 +2065,9 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
             const int j = j0 + 32 * u + lane;
             if (j < cntw) {
               lval[warp * WCAP + j] = lvv[u];
-              hist_e(Eof(lvv[u]));
+              const uint32_t bits = __float_as_uint(Eof(lvv[u]));
+              const int bn = ebin(bits);
+              if (bn <= bf) hist(bits, bn);  // a listed element of the partly listed bin: no
             }
           }
         }
@@ -2053,7 +2077,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     const bool fit = __syncthreads_and(cntw <= WCAP ? 1 : 0) != 0;
     // lists hold every element that can be kept (ids, logits)
     bool cand_lists = listing && fit;
-    if ((listing && !fit) || (PRE && trunc && !listing)) {
+    if ((listing && !fit) || (trunc && !listing)) {
       for (int k = threadIdx.x; k < kHist; k += NT) {
         hcnt[k] = 0u;
         hm[k] = 0u;
@@ -2062,15 +2086,9 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       sweep([&](int, float l) { hist_e(Eof(l)); });
       bf = -1;
     }
-    float zh, zl;
-    if constexpr (PRE) {
-      __syncthreads();  // the histogram and the Z pair are complete
-      zh = sh.zpre[0];
-      zl = sh.zpre[1];
-    } else {
-      zh = block_sum_f<NT>(zs, sh);  // includes barriers: histogram complete
-      zl = block_sum_f<NT>(-zc, sh);
-    }
+    __syncthreads();  // the histogram (and, PRE, the Z pair) is complete
+    const float zh = PRE ? sh.zpre[0] : zh_sw;
+    const float zl = PRE ? sh.zpre[1] : zl_sw;
     const float e_probe = sh.eprobe;
     const unsigned long long zfx = fx44_pair(zh, zl);  // Z in units of 2^-44
     // a draft row that is likely to reject (p(x) <= E(x) / Z_kept is not
