@@ -188,6 +188,22 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ the step on the GPU
+def step_splits(spec: wl.Spec, device, overlap: bool) -> int:
+    """The attention's split count in the step.  The library's own plan fills
+    one wave of SMs; when the sampler runs beside it as a few clusters (few
+    rows: one cluster of min(8, ceil(V / 16384)) CTAs per row) the attention
+    of a short block (at most 64 query rows per KV head: one row tile) is cut
+    into fewer splits, so that both fit on the SMs at once."""
+    if spec.num_splits or not overlap:
+        return spec.num_splits
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    samp_ctas = spec.B * spec.R * min(8, -(-spec.V // 16384))
+    units = spec.B * spec.Hkv
+    if samp_ctas > 2 * sms or spec.R * spec.Hq // spec.Hkv > 64 or units >= sms - samp_ctas:
+        return 0
+    return max(1, (sms - samp_ctas) // units)
+
+
 class GpuStep:
     """All buffers of one verify step, resident on the device."""
 
@@ -205,8 +221,9 @@ class GpuStep:
             else None
         self.pos = torch.empty((B, R), dtype=torch.int32, device=device)
         self.tst = torch.empty((B,), dtype=torch.int32, device=device)
+        self.splits = step_splits(spec, device, overlap)
         self.attn = sv.AttnCall(w.q, w.k_cache, w.v_cache, w.block_table, w.ctx_len, self.anc,
-                                num_splits=spec.num_splits)
+                                num_splits=self.splits)
         self.cfg = sv.SamplerConfig(temperature=spec.temperature, top_k=spec.top_k,
                                     top_p=spec.top_p, greedy=spec.greedy)
         self.sws = sv.new_workspace(sv.sample_workspace_size(B, R, spec.V), device)
@@ -376,7 +393,7 @@ def step_record(spec, step, t, nbytes, peak, ws, dev):
         "sampler_us": statistics.fmean(t["samp_ms"]) * 1e3 if t["samp_ms"] else None,
         "attn_num_splits": step.sv.attn_num_splits(
             spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
-            step.w.block_table.shape[1], spec.num_splits),
+            step.w.block_table.shape[1], step.splits),
     }
     if spec.is_tree or spec.R * spec.Hq // spec.Hkv >= 128:
         # a contraction-heavy shape: also against the bf16 tensor peak
