@@ -172,6 +172,32 @@ SPEC_DEV void mma_pv(uint32_t o, uint32_t pa, uint32_t vb, bool first) {
   }
 }
 
+// Packed pairs of fp32 (sm_100+ f32x2 arithmetic: one instruction, two lanes
+// of the pair, each rounded as the scalar operation would be).
+SPEC_DEV uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+SPEC_DEV void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+SPEC_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+SPEC_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+SPEC_DEV float fmax3(float a, float b, float c) {  // three-input maximum (sm_100+)
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Row state of one softmax thread.
 struct RowState {
   float m_run = -INFINITY;  // running maximum (log2 domain, scaled)
@@ -203,7 +229,9 @@ SPEC_DEV bool softmax_tile(const AttnParams& p, RowState& st, uint32_t s_addr, u
 #pragma unroll
   for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
-    for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[cb][c]));
+    for (int c = 0; c < 16; ++c)
+      m4[c & 3] = fmax3(m4[c & 3], __uint_as_float(sv[cb][2 * c]),
+                        __uint_as_float(sv[cb][2 * c + 1]));
   const float mnew = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
   const bool need = mnew > st.m_run + kRescaleLog2;
   float alpha = 1.f;
@@ -215,17 +243,25 @@ SPEC_DEV bool softmax_tile(const AttnParams& p, RowState& st, uint32_t s_addr, u
   // p = exp2(s * scale - m) and the row sum; P packed as bf16 pairs in place
   // (pair c of a 32-score block into word c), then written over the scores
   const float base = (st.m_run == -INFINITY) ? 0.f : st.m_run;
-  float rs[4] = {0.f, 0.f, 0.f, 0.f};
+  // the scaling of a score pair and the running sums in packed f32x2
+  const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nb2 = f2_pack(-base, -base);
+  uint64_t rs2[2] = {0ull, 0ull};  // +0.0f pairs
 #pragma unroll
   for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const float e0 = fast_exp2(fmaf(__uint_as_float(sv[cb][2 * c]), p.scale_log2, -base));
-      const float e1 = fast_exp2(fmaf(__uint_as_float(sv[cb][2 * c + 1]), p.scale_log2, -base));
-      rs[c & 3] += e0 + e1;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[cb][2 * c]), __uint_as_float(sv[cb][2 * c + 1])),
+                       sc2, nb2),
+                x0, x1);
+      const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+      rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(e0, e1));
       sv[cb][c] = pack_bf16(e0, e1);
     }
   }
+  float rs[4];
+  f2_unpack(rs2[0], rs[0], rs[1]);
+  f2_unpack(rs2[1], rs[2], rs[3]);
   bool ok = true;
   if (!first && __any_sync(0xffffffffu, need)) {
     // rescale this warp's rows of O once the previous PV has completed (after
