@@ -248,23 +248,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
     }
 
     // ---- scale, visibility mask, online softmax (log2 domain)
+    // (pairs e = 0, 1 and 2, 3 share a row: packed f32x2 arithmetic)
     const bool need_mask = tb + TS > ctx;
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+      float x[4];
+      f2_unpack(f2_mul(f2_pack(sacc[nt][0], sacc[nt][1]), sc2), x[0], x[1]);
+      f2_unpack(f2_mul(f2_pack(sacc[nt][2], sacc[nt][3]), sc2), x[2], x[3]);
+      if (need_mask) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = sacc[nt][e] * p.scale_log2;
-        if (need_mask) {
+        for (int e = 0; e < 4; ++e) {
           const int pos = tb + nt * 8 + cq + (e & 1);
           const uint64_t w = (e < 2) ? w0 : w1;
           const int j = pos - ctx;
           const bool vis = (pos < ctx) || (j < p.R && ((w >> j) & 1ull));
-          if (!vis) x = -INFINITY;
+          if (!vis) x[e] = -INFINITY;
         }
-        sacc[nt][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = x[e];
+      mx[0] = fmax3(mx[0], x[0], x[1]);
+      mx[1] = fmax3(mx[1], x[2], x[3]);
     }
     float base[2], alpha[2];
 #pragma unroll
@@ -276,16 +282,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
       alpha[h] = fast_exp2(m_run[h] - base[h]);  // exp2(-inf) = 0 on the first stage
       m_run[h] = mnew;
     }
-    float rs[2] = {0.f, 0.f};
+    const uint64_t nb0 = f2_pack(-base[0], -base[0]), nb1 = f2_pack(-base[1], -base[1]);
+    uint64_t rs2[2] = {0ull, 0ull};  // +0.0f pairs, one per row
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+      float d[4];
+      f2_unpack(f2_add(f2_pack(sacc[nt][0], sacc[nt][1]), nb0), d[0], d[1]);
+      f2_unpack(f2_add(f2_pack(sacc[nt][2], sacc[nt][3]), nb1), d[2], d[3]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = fast_exp2(sacc[nt][e] - base[e >> 1]);
-        sacc[nt][e] = pe;
-        rs[e >> 1] += pe;
-      }
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = fast_exp2(d[e]);
+      rs2[0] = f2_add(rs2[0], f2_pack(sacc[nt][0], sacc[nt][1]));
+      rs2[1] = f2_add(rs2[1], f2_pack(sacc[nt][2], sacc[nt][3]));
     }
+    float rs[2], r2a, r2b;
+    f2_unpack(rs2[0], r2a, r2b);
+    rs[0] = r2a + r2b;
+    f2_unpack(rs2[1], r2a, r2b);
+    rs[1] = r2a + r2b;
 #pragma unroll
     for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
     if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row maximum moved

@@ -172,32 +172,6 @@ SPEC_DEV void mma_pv(uint32_t o, uint32_t pa, uint32_t vb, bool first) {
   }
 }
 
-// Packed pairs of fp32 (sm_100+ f32x2 arithmetic: one instruction, two lanes
-// of the pair, each rounded as the scalar operation would be).
-SPEC_DEV uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-SPEC_DEV void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-SPEC_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-SPEC_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-SPEC_DEV float fmax3(float a, float b, float c) {  // three-input maximum (sm_100+)
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 // Row state of one softmax thread.
 struct RowState {
   float m_run = -INFINITY;  // running maximum (log2 domain, scaled)
