@@ -186,6 +186,19 @@ SPEC_DEV float fmax_nan(float a, float b) {
   return r;
 }
 
+// three-input maximum, NaN-propagating (sm_100+)
+SPEC_DEV float fmax3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+SPEC_DEV float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 SPEC_DEV float ex2_approx(float x) {
   float y;
   asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -1722,7 +1735,6 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   uint32_t* xbits = reinterpret_cast<uint32_t*>(xkey + NT);                          // NT
   int* lid = reinterpret_cast<int*>(xbits + NT);                                      // kSCap
   float* lval = reinterpret_cast<float*>(lid + kSCap);                                // kSCap
-  uint32_t* fbits = reinterpret_cast<uint32_t*>(lval + kSCap);  // (V + 31) / 32 when listing
   const RadixScratch rs{reinterpret_cast<uint32_t*>(xkey), xkey + 256, xkey + 768,
                         reinterpret_cast<uint32_t*>(xkey) + 2048};
   __shared__ Sh<NW> sh;
@@ -1825,6 +1837,7 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   RangeStat st{0.f, 0.f, 0.f, 0};
   float Lf = INFINITY;              // candidate floor (+inf: no lists)
   float zh_sw = 0.f, zl_sw = 0.f;   // Z of the sweep (relative to m), float pair
+  int cnt_sw = 0;                   // ids the sweep listed in this warp's range
   const float c_hi = p.c_hi, c_lo = p.c_lo, T150 = 150.f * p.T;
   if constexpr (PRE) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the pre-pass has completed
@@ -1835,6 +1848,11 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     Lf = p.lfloor[2 * row];
   } else {
     const float smp = ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol);
+    // the samples' bin counters (the members' scratch, unused until the cut)
+    uint32_t* scnt = reinterpret_cast<uint32_t*>(xkey);
+    static_assert(NT == kBins, "one counter per thread, and one more");
+    scnt[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) scnt[kBins] = 0u;
     float sm = smp;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sm = fmax_nan(sm, __shfl_xor_sync(kFull, sm, o));
@@ -1854,12 +1872,35 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           topk ? fminf((float)kSBudget, 4.f * (float)p.top_k + 1024.f) : (float)kSBudget;
       const int ns = (int)(budget * (float)NT / (float)V);
       if (ns >= 1 && (!topk || p.top_k <= kSBudget / 2)) {
-        const int sbin = ebin(__float_as_uint(Eref(smp)));
-        int lo = -1, hi = kBins - 1;  // the largest b with count(sample bin <= b) <= ns
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (__syncthreads_count(sbin <= mid) <= ns) lo = mid; else hi = mid - 1;
+        atomicAdd(&scnt[ebin(__float_as_uint(Eref(smp)))], 1u);
+        __syncthreads();
+        if (warp == 0) {  // the largest b with count(sample bin <= b) <= ns
+          uint32_t c = 0;
+          for (int b2 = 32 * lane; b2 < 32 * lane + 32; ++b2) c += scnt[b2];
+          uint32_t incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t2 = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t2;
+          }
+          const unsigned h = __ballot_sync(kFull, incl > (uint32_t)ns);
+          int bfs = kBins - 1;
+          if (h) {
+            const int L = __ffs(h) - 1;
+            uint32_t run = __shfl_sync(kFull, incl - c, L);
+            bfs = 32 * L + 31;
+            for (int b2 = 32 * L; b2 < 32 * L + 32; ++b2) {
+              run += scnt[b2];
+              if (run > (uint32_t)ns) {
+                bfs = b2 - 1;
+                break;
+              }
+            }
+          }
+          if (lane == 0) sh.bi[6] = bfs;
         }
+        __syncthreads();
+        const int lo = sh.bi[6];
         if (lo >= 0) Lf = sref - (float)(lo + 1) * (p.T * kLn2 * (1.f / 32.f));
       }
     }
@@ -1873,23 +1914,45 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       for (int u = 0; u < 4; ++u) {
         const int k = s0 + 128 * u + 4 * lane;
         float e[4];
+        mx = fmax3_nan(mx, lv[u][0], lv[u][1]);
+        mx = fmax3_nan(mx, lv[u][2], lv[u][3]);
+        if (FAST) {  // the exponents' arguments two at a time (packed f32x2 FMA)
+          const uint64_t c2 = f2_pack(c_hi, c_hi), n2 = f2_pack(snmc, snmc);
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(lv[u][0], lv[u][1]), c2, n2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(lv[u][2], lv[u][3]), c2, n2), x2, x3);
+          e[0] = ex2_ftz(x0);
+          e[1] = ex2_ftz(x1);
+          e[2] = ex2_ftz(x2);
+          e[3] = ex2_ftz(x3);  // 0 past the range
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          mx = fmax_nan(mx, lv[u][j]);
-          e[j] = Eref(lv[u][j]);  // 0 past the range
+          for (int j = 0; j < 4; ++j) e[j] = Eref(lv[u][j]);
         }
         const float y = ((e[0] + e[1]) + (e[2] + e[3])) - zc;  // Kahan
         const float t = zs + y;
         zc = (t - zs) - y;
         zs = t;
-        if (flagging) {  // a word of 32 consecutive ids per eight lanes
-          uint32_t nib = (lv[u][0] >= Lf ? 1u : 0u) | (lv[u][1] >= Lf ? 2u : 0u) |
-                         (lv[u][2] >= Lf ? 4u : 0u) | (lv[u][3] >= Lf ? 8u : 0u);
-          nib <<= 4 * (lane & 7);
-          nib |= __shfl_xor_sync(kFull, nib, 1);
-          nib |= __shfl_xor_sync(kFull, nib, 2);
-          nib |= __shfl_xor_sync(kFull, nib, 4);
-          if ((lane & 7) == 0 && k < r1) fbits[k >> 5] = nib;
+        if (flagging) {  // the ids at or above the floor, appended to the warp's list
+          bool f[4];
+          unsigned bal[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[j] = lv[u][j] >= Lf;  // false past the range (-inf)
+            bal[j] = __ballot_sync(kFull, f[j]);
+          }
+          int pos = cnt_sw + __popc(bal[0] & lt) + __popc(bal[1] & lt) + __popc(bal[2] & lt) +
+                    __popc(bal[3] & lt);  // ascending: lanes, then j
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (f[j]) {
+              if (pos < WCAP) {
+                lid[warp * WCAP + pos] = k + j;
+                lval[warp * WCAP + pos] = lv[u][j];
+              }
+              ++pos;
+            }
+          cnt_sw += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
         }
       }
     }
@@ -2030,46 +2093,14 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
       }
     } else if (listing) {
-      __syncwarp();  // the warp's flag words are written
-      const int w0 = (r0 + 31) >> 5, w1 = (r1 + 31) >> 5;  // r0: a multiple of 32, or V
-      for (int wb = w0; wb < w1; wb += 32) {
-        const int wd = wb + lane;
-        uint32_t word = wd < w1 ? fbits[wd] : 0u;
-        const int c = __popc(word);
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int t = __shfl_up_sync(kFull, incl, o);
-          if (lane >= o) incl += t;
-        }
-        int pos = cntw + incl - c;
-        while (word) {
-          const int bpos = __ffs(word) - 1;
-          word &= word - 1u;
-          if (pos < WCAP) lid[warp * WCAP + pos] = 32 * wd + bpos;
-          ++pos;
-        }
-        cntw += __shfl_sync(kFull, incl, 31);
-      }
+      // the sweep listed the ids at or above the floor with their logits
+      cntw = cnt_sw;
       if (cntw <= WCAP) {
         __syncwarp();
-        for (int j0 = 0; j0 < cntw; j0 += 512) {
-          float lvv[16];  // sixteen logits of the list in flight per lane
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = j0 + 32 * u + lane;
-            lvv[u] = j < cntw ? ldg_keep(lrow + lid[warp * WCAP + j], pol) : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = j0 + 32 * u + lane;
-            if (j < cntw) {
-              lval[warp * WCAP + j] = lvv[u];
-              const uint32_t bits = __float_as_uint(Eof(lvv[u]));
-              const int bn = ebin(bits);
-              if (bn <= bf) hist(bits, bn);  // a listed element of the partly listed bin: no
-            }
-          }
+        for (int j = lane; j < cntw; j += 32) {
+          const uint32_t bits = __float_as_uint(Eof(lval[warp * WCAP + j]));
+          const int bn = ebin(bits);
+          if (bn <= bf) hist(bits, bn);  // a listed element of the partly listed bin: no
         }
       }
     }
@@ -2992,8 +3023,8 @@ spec_status launch_nt(const SP& prm, const SampPlan& pl, int rows, cudaStream_t 
 }
 
 size_t stream_smem(int V) {
-  const size_t words = V <= kSListMaxV ? (size_t)(V + 31) / 32 : 0;
-  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8 + words * 4;
+  (void)V;
+  return 2 * (size_t)kHistPad * 4 + (size_t)kSNT * 12 + (size_t)kSCap * 8;
 }
 
 // the row kernel, after the pre-pass when PRE (a programmatic dependent: its
