@@ -167,6 +167,12 @@ SPEC_DEV uint64_t l2_keep_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// L2 policy for data read once
+SPEC_DEV uint64_t l2_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 SPEC_DEV float4 ldg_keep4(const float4* p, uint64_t pol) {
   float4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
@@ -1751,7 +1757,8 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
   const bool vec = p.bulk != 0;  // V % 4 == 0 and 16-byte aligned rows
   const int n4 = vec ? V / 4 : 0;
   const float4* l4 = reinterpret_cast<const float4*>(lrow);
-  const uint64_t pol = l2_keep_policy();
+  // the row is swept once (the lists keep what the cut needs): L2 need not keep it
+  const uint64_t pol = PRE ? l2_keep_policy() : l2_first_policy();
   // every element of the row once: visit(k, l), four 16-byte loads in flight per thread
   auto sweep = [&](auto&& visit) {
     for (int base = threadIdx.x; base < n4; base += 4 * NT) {
@@ -1907,6 +1914,10 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     const bool flagging = Lf < INFINITY;
     float mx = -INFINITY, zs = 0.f, zc = 0.f;
     for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
+      // the chunk after the next one into L2 now (one 128-byte line per lane of
+      // the first 16): the loads below then wait on L2 rather than on HBM
+      if (lane < 16 && s0 + 1024 + 32 * lane < r1)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(lrow + s0 + 1024 + 32 * lane));
       float lv[4][4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) load4(s0 + 128 * u + 4 * lane, lv[u]);
@@ -2647,12 +2658,6 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 constexpr int kSwMaxPieces = 64;  // 128-id pieces per range (ranges of up to 8192 ids)
 constexpr int kSwCTAs = 5;        // pre-pass CTAs per SM (two range buffers each)
 
-// L2 policy for data read once (the logits in the pre-pass)
-SPEC_DEV uint64_t l2_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
 
 // The row's candidate floor as a logit (+inf: no lists).  Every thread
 // returns the same value; contains barriers (call from uniform control flow).
