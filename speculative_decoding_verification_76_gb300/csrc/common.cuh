@@ -140,17 +140,7 @@ SPEC_DEV uint32_t dsmem_addr(const void* local, uint32_t rank) {
   return out;
 }
 
-SPEC_DEV float dsmem_ld_f32(const void* local, uint32_t rank) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(local, rank)) : "memory");
-  return v;
-}
 
-SPEC_DEV double dsmem_ld_f64(const void* local, uint32_t rank) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(dsmem_addr(local, rank)) : "memory");
-  return v;
-}
 
 SPEC_DEV uint32_t dsmem_ld_u32(const void* local, uint32_t rank) {
   uint32_t v;
