@@ -188,20 +188,28 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ the step on the GPU
-def step_splits(spec: wl.Spec, device, overlap: bool) -> int:
+def step_splits(spec: wl.Spec, device, overlap: bool, max_pages: int) -> int:
     """The attention's split count in the step.  The library's own plan fills
     one wave of SMs; when the sampler runs beside it as a few clusters (few
     rows: one cluster of min(8, ceil(V / 16384)) CTAs per row) the attention
     of a short block (at most 64 query rows per KV head: one row tile) is cut
-    into fewer splits, so that both fit on the SMs at once."""
+    into fewer splits, so that both fit on the SMs at once (the library rounds
+    an explicit count to its chunk granularity: the largest request whose
+    plan fits is taken)."""
     if spec.num_splits or not overlap:
         return spec.num_splits
+    import speculative_decoding_verification_76_gb300 as sv
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     samp_ctas = spec.B * spec.R * min(8, -(-spec.V // 16384))
     units = spec.B * spec.Hkv
     if samp_ctas > 2 * sms or spec.R * spec.Hq // spec.Hkv > 64 or units >= sms - samp_ctas:
         return 0
-    return max(1, (sms - samp_ctas) // units)
+    for req in range((sms - samp_ctas) // units, 0, -1):
+        got = sv.attn_num_splits(spec.B, spec.R, spec.Hq, spec.Hkv, spec.D, spec.page_size,
+                                 max_pages, req)
+        if 0 < got * units <= sms - samp_ctas:
+            return req
+    return 0
 
 
 class GpuStep:
@@ -221,7 +229,7 @@ class GpuStep:
             else None
         self.pos = torch.empty((B, R), dtype=torch.int32, device=device)
         self.tst = torch.empty((B,), dtype=torch.int32, device=device)
-        self.splits = step_splits(spec, device, overlap)
+        self.splits = step_splits(spec, device, overlap, w.block_table.shape[1])
         self.attn = sv.AttnCall(w.q, w.k_cache, w.v_cache, w.block_table, w.ctx_len, self.anc,
                                 num_splits=self.splits)
         self.cfg = sv.SamplerConfig(temperature=spec.temperature, top_k=spec.top_k,
