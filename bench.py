@@ -542,7 +542,7 @@ def bench_e2e(step: GpuStep, spec, n, ws, dev):
             dst[k].copy_(host[k], non_blocking=True)
         anc = sv.tree_prepare(dst["parent"], dst["ctx_len"])[0] if spec.is_tree else None
         sv.verify_attn(dst["q"], w.k_cache, w.v_cache, dst["block_table"], dst["ctx_len"], anc,
-                       num_splits=spec.num_splits, workspace=step.attn.workspace)
+                       num_splits=step.splits, workspace=step.attn.workspace)
         if spec.is_tree:
             r = sv.accept_sample_tree(dst["logits"], dst["draft_probs"], dst["draft_tokens"],
                                       dst["parent"], dst["uniforms"], cfg, workspace=step.sws)
