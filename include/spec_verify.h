@@ -119,7 +119,7 @@ spec_status spec_tree_prepare(const int32_t* parent, const int32_t* ctx_len, int
  *
  * Query head h reads KV head h / (Hq/Hkv).  Supported: D in {64,128};
  * bf16 needs D == 128, page_size % 16 == 0, 16-byte aligned cache rows;
- * fp32 any page_size; R*Hq/Hkv <= 512; R <= 64.
+ * fp32 any page_size; R*Hq/Hkv <= 512; R <= 64; B <= 65535.
  * ---------------------------------------------------------------------- */
 size_t spec_verify_attn_workspace_size(int B, int R, int Hq, int Hkv, int D, int page_size,
                                        int max_pages, int num_splits);

@@ -719,6 +719,7 @@ spec_status verify_attn_impl(const void* q, const void* k_cache, const void* v_c
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EINVAL;
   if (B == 0) return SPEC_OK;
   if (R > 64 || (D != 64 && D != 128)) return SPEC_EUNSUPPORTED;
+  if (B > 65535) return SPEC_EUNSUPPORTED;  // sequences index the grid's z dimension
   const bool bf16 = dtype == SPEC_BF16;
   if (bf16 && (D != 128 || page_size % 16 != 0 || R * (Hq / Hkv) > 512)) return SPEC_EUNSUPPORTED;
   if ((phase & kPartials) && bf16 &&
