@@ -1912,7 +1912,11 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       }
     }
     const bool flagging = Lf < INFINITY;
-    float mx = -INFINITY, zs = 0.f, zc = 0.f;
+    float mx = -INFINITY;
+    uint64_t zs2 = f2_pack(0.f, 0.f), zc2 = f2_pack(0.f, 0.f);
+    const uint64_t m1 = f2_pack(-1.f, -1.f);
+    int* const wlid = lid + warp * WCAP;
+    float* const wlval = lval + warp * WCAP;
     for (int s0 = r0; s0 < r1; s0 += 512) {  // warp-uniform
       // the chunk after the next one into L2 now (one 128-byte line per lane of
       // the first 16): the loads below then wait on L2 rather than on HBM
@@ -1940,10 +1944,11 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) e[j] = Eref(lv[u][j]);
         }
-        const float y = ((e[0] + e[1]) + (e[2] + e[3])) - zc;  // Kahan
-        const float t = zs + y;
-        zc = (t - zs) - y;
-        zs = t;
+        // Kahan summation of (e0 + e2, e1 + e3) in two packed streams
+        const uint64_t y2 = f2_fma(zc2, m1, f2_add(f2_pack(e[0], e[1]), f2_pack(e[2], e[3])));
+        const uint64_t t2 = f2_add(zs2, y2);
+        zc2 = f2_fma(y2, m1, f2_fma(zs2, m1, t2));  // (t - s) - y
+        zs2 = t2;
         if (flagging) {  // the ids at or above the floor, appended to the warp's list
           bool f[4];
           unsigned bal[4];
@@ -1954,16 +1959,26 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           }
           int pos = cnt_sw + __popc(bal[0] & lt) + __popc(bal[1] & lt) + __popc(bal[2] & lt) +
                     __popc(bal[3] & lt);  // ascending: lanes, then j
+          if (cnt_sw + 128 <= WCAP) {  // warp-uniform: every entry of the group fits
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (f[j]) {
-              if (pos < WCAP) {
-                lid[warp * WCAP + pos] = k + j;
-                lval[warp * WCAP + pos] = lv[u][j];
+            for (int j = 0; j < 4; ++j)
+              if (f[j]) {
+                wlid[pos] = k + j;
+                wlval[pos] = lv[u][j];
+                ++pos;
               }
-              ++pos;
-            }
-          cnt_sw += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (f[j]) {
+                if (pos < WCAP) {
+                  wlid[pos] = k + j;
+                  wlval[pos] = lv[u][j];
+                }
+                ++pos;
+              }
+          }
+          cnt_sw = __shfl_sync(kFull, pos, 31);  // the last lane's end: the warp's count
         }
       }
     }
@@ -1975,6 +1990,18 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     m = sh.red_f[0];
     for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.red_f[w]);
     __syncthreads();  // every thread has m before the sums reuse sh.red_f
+    float zs, zc;
+    {
+      float s0, s1, c0, c1;
+      f2_unpack(zs2, s0, s1);
+      f2_unpack(zc2, c0, c1);
+      // the streams' sums added exactly (TwoSum: zs + err), the compensations
+      // (excess over the true sums) added in
+      zs = s0 + s1;
+      const float bb = zs - s0;
+      const float err = (s0 - (zs - bb)) + (s1 - bb);
+      zc = (c0 + c1) - err;
+    }
     const float Zh = block_sum_f<NT>(zs, sh), Zl = block_sum_f<NT>(-zc, sh);
     if (fabsf(m) < INFINITY) {  // uniform
       if (sref_ok && fabsf(Zh) < INFINITY) {
