@@ -1782,6 +1782,19 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     for (int k = 4 * n4 + threadIdx.x; k < V; k += NT) visit(k, ldg_keep(lrow + k, pol));
   };
   int ph = 0;
+  // the floor's sample (one per thread, evenly spaced) and the first 8 KB of
+  // each warp's id range are requested before the setup: their latency hides
+  // under it
+  const float smp =
+      PRE ? 0.f : ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol);
+  if (!PRE) {
+    const int rw0 = stream_range_width(V);
+    const int a0 = min(warp * rw0, V), a1 = min((warp + 1) * rw0, V);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (a0 + 1024 * q + 32 * lane < a1)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(lrow + a0 + 1024 * q + 32 * lane));
+  }
 
   // ---- 0. setup
   if (threadIdx.x == 0) {
@@ -1854,7 +1867,6 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
     for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
     Lf = p.lfloor[2 * row];
   } else {
-    const float smp = ldg_keep(lrow + (int)(((long long)threadIdx.x * V) / NT), pol);
     // the samples' bin counters (the members' scratch, unused until the cut)
     uint32_t* scnt = reinterpret_cast<uint32_t*>(xkey);
     static_assert(NT == kBins, "one counter per thread, and one more");
@@ -1882,8 +1894,14 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         atomicAdd(&scnt[ebin(__float_as_uint(Eref(smp)))], 1u);
         __syncthreads();
         if (warp == 0) {  // the largest b with count(sample bin <= b) <= ns
+          // lane o: the count of octave o (bins 32 o .. 32 o + 31, 16-byte loads)
+          const uint4* s4 = reinterpret_cast<const uint4*>(scnt + 32 * lane);
           uint32_t c = 0;
-          for (int b2 = 32 * lane; b2 < 32 * lane + 32; ++b2) c += scnt[b2];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = s4[v];
+            c += (x.x + x.y) + (x.z + x.w);
+          }
           uint32_t incl = c;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -1893,16 +1911,19 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
           const unsigned h = __ballot_sync(kFull, incl > (uint32_t)ns);
           int bfs = kBins - 1;
           if (h) {
+            // the crossing octave L: lane j takes bin 32 L + j, the running
+            // count over the octave by a warp scan
             const int L = __ffs(h) - 1;
-            uint32_t run = __shfl_sync(kFull, incl - c, L);
-            bfs = 32 * L + 31;
-            for (int b2 = 32 * L; b2 < 32 * L + 32; ++b2) {
-              run += scnt[b2];
-              if (run > (uint32_t)ns) {
-                bfs = b2 - 1;
-                break;
-              }
+            const uint32_t base = __shfl_sync(kFull, incl - c, L);
+            const uint32_t v = scnt[32 * L + lane];
+            uint32_t run = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t t2 = __shfl_up_sync(kFull, run, o);
+              if (lane >= o) run += t2;
             }
+            const unsigned h2 = __ballot_sync(kFull, base + run > (uint32_t)ns);
+            bfs = 32 * L + (__ffs(h2) - 1) - 1;  // h2 != 0: the octave's total crosses ns
           }
           if (lane == 0) sh.bi[6] = bfs;
         }
