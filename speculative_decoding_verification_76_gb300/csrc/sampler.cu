@@ -1000,8 +1000,17 @@ SPEC_DEV bool select_cut(unsigned long long key, uint32_t eb, int total, unsigne
     }
     __syncthreads();
     int rank = 0;
-    if (t < total)
-      for (int j = 0; j < total; ++j) rank += xkey[j] > key ? 1 : 0;
+    if (t < total) {
+      // four independent counts: the shared-memory loads overlap
+      int r4[4] = {0, 0, 0, 0};
+      int j = 0;
+      for (; j + 4 <= total; j += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) r4[u] += xkey[j + u] > key ? 1 : 0;
+      }
+      for (; j < total; ++j) r4[0] += xkey[j] > key ? 1 : 0;
+      rank = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+    }
     __syncthreads();
     if (t < total) {
       xkey[rank] = key;
@@ -2156,10 +2165,22 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
       cntw = cnt_sw;
       if (cntw <= WCAP) {
         __syncwarp();
-        for (int j = lane; j < cntw; j += 32) {
-          const uint32_t bits = __float_as_uint(Eof(lval[warp * WCAP + j]));
-          const int bn = ebin(bits);
-          if (bn <= bf) hist(bits, bn);  // a listed element of the partly listed bin: no
+        const float* wv = lval + warp * WCAP;
+        for (int j0 = 0; j0 < cntw; j0 += 128) {  // four entries per lane in flight
+          float lv4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u + lane;
+            lv4[u] = j < cntw ? wv[j] : -INFINITY;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (j0 + 32 * u + lane < cntw) {
+              const uint32_t bits = __float_as_uint(Eof(lv4[u]));
+              const int bn = ebin(bits);
+              if (bn <= bf) hist(bits, bn);  // a listed element of the partly listed bin: no
+            }
+          }
         }
       }
     }
@@ -2311,7 +2332,21 @@ __global__ void __launch_bounds__(kSNT, 1) sampler_stream_kernel(const SP p) {
         }
         if (cand_lists) {
           const int cnt = sh.list_n[warp];
-          for (int j = lane; j < cnt; j += 32) consider(lid[warp * WCAP + j], lval[warp * WCAP + j]);
+          const int* wi = lid + warp * WCAP;
+          const float* wv = lval + warp * WCAP;
+          for (int j0 = 0; j0 < cnt; j0 += 128) {  // four entries per lane in flight
+            int id4[4];
+            float lv4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = j0 + 32 * u + lane;
+              id4[u] = j < cnt ? wi[j] : 0;
+              lv4[u] = j < cnt ? wv[j] : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (j0 + 32 * u + lane < cnt) consider(id4[u], lv4[u]);
+          }
         } else {
           // the row, each warp its range, 32 consecutive ids per step, eight
           // steps' loads in flight
