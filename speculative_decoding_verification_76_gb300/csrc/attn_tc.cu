@@ -464,8 +464,8 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
 // ============================================================== NM = 2
 namespace two {
 constexpr int kStages = 2;
-constexpr int kSoftWarps = 8, kMmaWarp = 8, kCopyWarp0 = 10;  // MMA warps 8 (tile 0), 9 (tile 1)
-constexpr int kThreads = 32 * (kSoftWarps + 2 + kCopyWarps);
+constexpr int kSoftWarps = 8, kMmaWarp = 8, kCopyWarp0 = 9;
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kCopyWarps);
 // tensor memory: score / P buffer of tile m at 128 m, O of tile m at 256 + 128 m
 constexpr int kColS = 0, kColO = 256;
 constexpr int kOffQ = kStages * kStageBytes;  // 2 x (Q lo 16 KB + Q hi 16 KB)
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], kCopyThreads);
-      mbar_init(&kv_empty[i], 2);  // each tile's MMA thread, once its PV of the stage is done
+      mbar_init(&kv_empty[i], 1);
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&s_full[m], 1);
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
       mbar_init(&o_done[m], 1);
     }
     mbar_init(q_full, 1);
-    mbar_init(mma_done, 2);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -526,10 +526,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
 
   if (warp >= kCopyWarp0) {
     copy_stages<kStages>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // one MMA thread per row tile: each tile's chain S_m(j) -> softmax -> PV_m(j)
-    // -> S_m(j+1) runs on its own, the tensor pipe interleaving the two
-    const int m = warp - kMmaWarp;
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, p.err, p.wait_ns);
       tc_fence_after();
@@ -539,17 +536,29 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
         if (!mbar_wait(&kv_full[slot], (j / kStages) & 1, p.err, p.wait_ns)) break;
         fence_proxy_async();  // the copy warps' generic-proxy writes, seen by the tensor cores
         const uint32_t kb = smem_u32(stages + slot * kStageBytes);
-        // S_m(j) once PV_m(j-1) has read P_m(j-1)
-        if (j >= 1 && !mbar_wait(&o_done[m], (j - 1) & 1, p.err, p.wait_ns)) break;
-        tc_fence_after();
-        mma_scores(tmem + kColS + m * kST, false, 0, q0 + m * 32768, kb);
-        tc_commit(&s_full[m]);
-        // O_m += P_m(j) V_j
-        if (!mbar_wait(&p_full[m], j & 1, p.err, p.wait_ns)) break;
-        tc_fence_after();
-        mma_pv(tmem + kColO + m * 128, tmem + kColS + m * kST, kb + 2 * kHalf, j == 0);
-        tc_commit(&o_done[m]);
-        tc_commit(&kv_empty[slot]);  // this tile's use of the stage ends with these MMAs
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // S_m(j) once PV_m(j-1) has read P_m(j-1)
+          if (j >= 1 && !mbar_wait(&o_done[m], (j - 1) & 1, p.err, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_scores(tmem + kColS + m * kST, false, 0, q0 + m * 32768, kb);
+          tc_commit(&s_full[m]);
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // O_m += P_m(j) V_j
+          if (!mbar_wait(&p_full[m], j & 1, p.err, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_pv(tmem + kColO + m * 128, tmem + kColS + m * kST, kb + 2 * kHalf, j == 0);
+          tc_commit(&o_done[m]);
+        }
+        if (!ok) break;
+        tc_commit(&kv_empty[slot]);  // the stage is free once these MMAs complete
       }
       tc_commit(mma_done);  // every issued MMA completes before tensor memory is freed
       mbar_wait(mma_done, 0, nullptr);  // never cut short: TMEM is freed next
