@@ -305,13 +305,21 @@ def time_step(step: GpuStep, steps: int, warmup: int, flush_l2, ws: int, gpu_ind
     for _ in range(3):                     # eager warm-up: attributes, descriptors
         step.run()
     torch.cuda.synchronize()
-    try:   # events captured as graph nodes time the partial pass and the sampler
+    # the timed graph holds the step's kernels only; a second graph of the same
+    # step with event-record nodes (which lengthen a replay by ~10 us) gives the
+    # partial pass's and the sampler's spans inside the step, after the timed region
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run()
+    try:
         ev_in = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
     except TypeError:
         ev_in = None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step.run(ev_in)
+    graph_ev = None
+    if ev_in is not None:
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
+            step.run(ev_in)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ms, part_ms, samp_ms = [], [], []
@@ -331,15 +339,21 @@ def time_step(step: GpuStep, steps: int, warmup: int, flush_l2, ws: int, gpu_ind
             e1.record(stream)
             e1.synchronize()
             step_ms.append(e0.elapsed_time(e1))
-            if ev_in is not None:
-                part_ms.append(ev_in[0].elapsed_time(ev_in[1]))
-                samp_ms.append(ev_in[2].elapsed_time(ev_in[3]))
         torch.cuda.synchronize()
         barrier(ws)
     finally:
         if clk:
             clk.__exit__()
-    if ev_in is None:   # no graph event nodes: time the partial pass eagerly
+    if graph_ev is not None:
+        for i in range(min(steps, 200) + 3):
+            flush_l2()
+            graph_ev.replay()
+            ev_in[3].synchronize()
+            torch.cuda.synchronize()
+            if i >= 3:
+                part_ms.append(ev_in[0].elapsed_time(ev_in[1]))
+                samp_ms.append(ev_in[2].elapsed_time(ev_in[3]))
+    else:   # no graph event nodes: time the partial pass eagerly
         for _ in range(min(steps, 200)):
             flush_l2()
             e0.record(stream)
