@@ -533,7 +533,8 @@ def arm_config(spec, seq_len, ws):
         "greedy": spec.greedy, "draft_noise": spec.draft_noise, "parallelism": f"replicas{ws}",
         "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read of a second "
               "buffer; outside the timed events)",
-        "timing": "CUDA-graph replay, CUDA events per step"}
+        "timing": ("CUDA-graph replay of the step's kernels, CUDA events per step; the phase "
+                   "spans from a second graph with event-record nodes")}
 
 
 def bench_e2e(step: GpuStep, spec, n, ws, dev):
