@@ -630,9 +630,12 @@ def bench_e2e(step: GpuStep, spec, n, ws, dev):
         one()
     dt = (time.perf_counter() - t0) / n
     dt = max_over_ranks(dt, ws, device=dev)
+    # the same inputs and uniforms: the host copies of the results equal the
+    # device-resident step's (the graph replays above left them in step.sout)
+    same = all(torch.equal(res_host[k], step.sout[k].cpu()) for k in res_host)
     return {"value": sum_over_ranks(spec.B * spec.R, ws, device=dev) / dt, "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": dt * 1e3, "steps": n,
+            "ms_per_step": dt * 1e3, "steps": n, "results_match_step": bool(same),
             "note": ("KV cache resident in HBM; per-step inputs copied from pinned host "
                      + ("memory (the sampler's in 4 batch slices on a copy stream, each "
                         "sampled on a third stream once it has landed; the attention under "

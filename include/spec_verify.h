@@ -245,18 +245,21 @@ typedef struct {
 } spec_sampler;
 
 /* Workspace of spec_accept_sample / _tree for B sequences of R rows (N
- * nodes) over a vocabulary of V; 0 for invalid sizes.
+ * nodes) over a vocabulary of V; 0 for invalid sizes.  The per-sequence
+ * counters sit at one place for every shape (room for 65536 sequences after
+ * the 256-byte error header), so a zero-filled workspace serves any later
+ * call whose own size fits in it, whatever its B, R or V.
  *
  * When many rows are sampled at once (B R cluster(V) > 2 x the SM count,
  * cluster(V) = min(8, ceil(V / 16384))) with truncation, each row is handled
- * by one CTA that sweeps it twice (maximum, then Z and a candidate list).
- * A workspace of spec_accept_sample_workspace_size_two_pass(B, R, V) bytes
- * (about 260 KB per row more) selects the two-pass variant instead: a
- * pre-pass sweeps every row from HBM once over all SMs (maximum, Z and the
- * candidate list of each warp range), then one CTA per row finishes it.  The
- * results are the same.  Alone the two-pass variant is slightly faster; next
- * to concurrent HBM-bound work (the verify step's attention) the one-kernel
- * variant is, so it is the default. */
+ * by one CTA that sweeps it once (maximum, Z and a candidate list of the ids
+ * at or above a sampled floor) and works on the list.  A workspace of
+ * spec_accept_sample_workspace_size_two_pass(B, R, V) bytes (about 260 KB
+ * per row more) selects the two-pass variant instead: a pre-pass sweeps
+ * every row from HBM once over all SMs (maximum, Z and the candidate list of
+ * each warp range), then one CTA per row finishes it.  The results are the
+ * same; the one-kernel variant is the faster one, alone and next to
+ * concurrent HBM-bound work, so it is the default. */
 size_t spec_accept_sample_workspace_size(int B, int R, int V);
 size_t spec_accept_sample_workspace_size_two_pass(int B, int R, int V);
 
@@ -282,7 +285,7 @@ size_t spec_accept_sample_workspace_size_two_pass(int B, int R, int V);
  * A token is accepted iff u*q(x) < p(x) (the event u < min(1, p/q)); the
  * correction is the first id t whose ascending running sum of
  * max(0, p - q) exceeds u_final * sum; the bonus draws from p the same way.
- * 1 <= R <= 64, 1 <= V <= 172032.
+ * 1 <= B <= 65536, 1 <= R <= 64, 1 <= V <= 172032.
  * ---------------------------------------------------------------------- */
 spec_status spec_accept_sample(const float* target_logits, const float* draft_probs,
                                const int32_t* draft_tokens, const float* uniforms,
@@ -308,7 +311,7 @@ spec_status spec_accept_sample(const float* target_logits, const float* draft_pr
  *   accepted_len  [B] out: accepted nodes on the path.
  *   path_nodes    [B,N] out: accepted node ids, then -1.
  *   emitted       [B,N] out: accepted tokens then the final token, then -1.
- *   p_out, status_per_seq as above.  2 <= N <= 64.
+ *   p_out, status_per_seq as above.  1 <= B <= 65536, 2 <= N <= 64.
  * ---------------------------------------------------------------------- */
 spec_status spec_accept_sample_tree(const float* target_logits, const float* draft_probs,
                                     const int32_t* node_tokens, const int32_t* parent,

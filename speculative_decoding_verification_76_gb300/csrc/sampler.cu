@@ -3055,15 +3055,20 @@ struct SampWs {
   size_t out, cnt, stats, lfloor, lid, lval, segcnt, end;
 };
 
+// Sequences per call.  The per-sequence counters sit at one place for every
+// shape, right after the header: a completed call leaves them at zero, so a
+// workspace serves later calls of any batch size or block length.
+constexpr int kMaxSeqs = 65536;
+
 SampWs samp_ws(int B, int R, bool pre) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = (size_t)B * R;
   SampWs w;
   size_t off = sizeof(WsHeader);
+  w.cnt = off;
+  off += up((size_t)kMaxSeqs * sizeof(int32_t));
   w.out = off;
   off += up(rows * sizeof(Outcome));
-  w.cnt = off;
-  off += up((size_t)B * sizeof(int32_t));
   w.stats = w.lfloor = w.lid = w.lval = w.segcnt = 0;
   if (pre) {
     w.stats = off;
@@ -3279,7 +3284,7 @@ extern "C" spec_status spec_accept_sample(const float* target_logits, const floa
   if (!target_logits || !accepted_len || !emitted || !workspace) return SPEC_EINVAL;
   if (R > 1 && !draft_tokens) return SPEC_EINVAL;
   if (!cfg->greedy && (!uniforms || (R > 1 && !draft_probs))) return SPEC_EINVAL;
-  if (R > kMaxN || (long long)B * R * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
+  if (R > kMaxN || B > kMaxSeqs || (long long)B * R * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
   if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
   if (workspace_bytes < samp_ws(B, R, false).end) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;
@@ -3309,7 +3314,7 @@ extern "C" spec_status spec_accept_sample_tree(const float* target_logits,
       !workspace)
     return SPEC_EINVAL;
   if (!cfg->greedy && (!uniforms || !draft_probs)) return SPEC_EINVAL;
-  if (N > kMaxN || (long long)B * N * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
+  if (N > kMaxN || B > kMaxSeqs || (long long)B * N * kMaxCS > INT_MAX) return SPEC_EUNSUPPORTED;
   if (!slice_fits(V)) return SPEC_EUNSUPPORTED;
   if (workspace_bytes < samp_ws(B, N, false).end) return SPEC_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SPEC_EINVAL;

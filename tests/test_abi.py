@@ -119,6 +119,21 @@ def test_workspace_sizes(lib):
     assert big >= mn + 320 * (32 * 16 + 32 * 8 * 128 * 8 + 32 * 8 * 4 + 8)
     assert sv.sample_workspace_size(64, 5, 0) == 0          # no vocabulary: invalid
     assert sv.sample_workspace_size(64, 5, 0, True) == 0
+    # the per-sequence counters have one place for every shape (65536 of them
+    # after the 256-byte header); the rest grows with the rows
+    one = sv.sample_workspace_size(1, 1, 100)
+    assert one >= 256 + 65536 * 4
+    assert sv.sample_workspace_size(64, 5, 100) - one < 64 * 5 * 16 + 256
+
+
+def test_sampler_batch_limit_refused_on_host(lib):
+    # more than 65536 sequences: refused before any launch (no device pointer
+    # is touched, so dummy addresses do)
+    p = ctypes.c_void_p(256)
+    c = api.SamplerConfig().c()
+    rc = lib.spec_accept_sample(p, p, p, p, 65537, 2, 100, ctypes.byref(c), p, 1 << 40, p, p,
+                                None, None, None)
+    assert rc == api.SPEC_EUNSUPPORTED
 
 
 def test_kv_commit_host_validation(lib):

@@ -291,6 +291,52 @@ def test_batched_serving_topp_sample():
             compare(gpu2, ref)
 
 
+def test_workspace_reuse_across_shapes():
+    """One zero-filled workspace serves calls of different shapes in turn: a
+    full batch on the many-row path, the same sequences in slices (many-row
+    and cluster paths, outputs written through offset views), a tree call of
+    another block length, then the full batch again.  Every result equals the
+    full batch's on a fresh workspace."""
+    spec = wl.SPECS["batched_serving_a75"].with_(B=16)
+    w = wl.make_sampler_inputs(spec, seed=5, device=DEV)
+    cfg = _api_cfg(cfg_of(spec))
+    tspec = wl.Spec("tree", B=24, Hq=1, Hkv=1, D=64, V=2000, ctx=(1, 1), tree_nodes=20,
+                    tree_depth=4, temperature=0.7, top_k=8, draft_div=0.7, draft_noise=0.5)
+    tw = wl.make_sampler_inputs(tspec, seed=1, device=DEV)
+    size = max(sv.sample_workspace_size(16, spec.R, spec.V),
+               sv.sample_workspace_size(24, tspec.R, tspec.V))
+
+    def full(ws):
+        r = sv.accept_sample(w.logits, w.draft_probs, w.draft_tokens, w.uniforms, cfg,
+                             workspace=ws)
+        torch.cuda.synchronize()
+        return {k: v.cpu() for k, v in r.items()}
+
+    ref = full(sv.new_workspace(size, DEV))
+    ws = sv.new_workspace(size, DEV)
+    assert all(torch.equal(ref[k], v) for k, v in full(ws).items())
+    for cb in (8, 2):   # B = 8: the many-row path; B = 2: the cluster path
+        out = {k: torch.full_like(v, -7, device=DEV) for k, v in ref.items()}
+        for c in range(16 // cb):
+            sl = slice(c * cb, (c + 1) * cb)
+            sv.accept_sample(w.logits[sl], w.draft_probs[sl], w.draft_tokens[sl],
+                             w.uniforms[sl], cfg, workspace=ws,
+                             out={k: v[sl] for k, v in out.items()})
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(ref[k], out[k].cpu()), (cb, k)
+    tref = sv.accept_sample_tree(tw.logits, tw.draft_probs, tw.draft_tokens, tw.parent,
+                                 tw.uniforms, _api_cfg(cfg_of(tspec)),
+                                 workspace=sv.new_workspace(size, DEV))
+    tgot = sv.accept_sample_tree(tw.logits, tw.draft_probs, tw.draft_tokens, tw.parent,
+                                 tw.uniforms, _api_cfg(cfg_of(tspec)), workspace=ws)
+    torch.cuda.synchronize()
+    for k in tref:
+        assert torch.equal(tref[k].cpu(), tgot[k].cpu()), k
+    assert all(torch.equal(ref[k], v) for k, v in full(ws).items())
+    assert sv.workspace_error(ws) == 0
+
+
 @pytest.mark.parametrize("name", ["batched_serving_a45", "batched_serving_a75"])
 def test_batched_serving_full_size(name):
     """The bench's sampler launch at full size: B = 64 sequences, 320 rows of
