@@ -140,6 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
     const uint8_t* vcol = reinterpret_cast<const uint8_t*>(p.v) + (size_t)kvh * 256 + c4 * 64;
     const bool pow2 = (P & (P - 1)) == 0;
     const int pshift = __ffs(P) - 1;
+    // K/V rows are read once (the CTAs of one chunk are its only readers):
+    // first out of L2, so that the partials and the block tables stay
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     for (int k = 0; k < nst; ++k) {
       const int slot = k % kNumStages;
       if (k >= kNumStages && !mbar_wait(&empty[slot], ((k / kNumStages) - 1) & 1, p.err, p.wait_ns)) break;
@@ -162,11 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_bf16(const AttnParam
         const uint8_t* vs = vcol + row;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(drow + col[u]),
-                       "l"(ks + 16 * u), "r"(n)
+          asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                           drow + col[u]),
+                       "l"(ks + 16 * u), "r"(n), "l"(pol)
                        : "memory");
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(drow + col[u] + 2 * H),
-                       "l"(vs + 16 * u), "r"(n)
+          asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                           drow + col[u] + 2 * H),
+                       "l"(vs + 16 * u), "r"(n), "l"(pol)
                        : "memory");
         }
       }

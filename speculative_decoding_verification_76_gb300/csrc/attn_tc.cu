@@ -76,8 +76,9 @@ SPEC_DEV Chunk chunk_of(const AttnParams& p) {
 }
 
 // Copy warps: the chunk's block-table slice, then its K/V stages into a ring
-// of NS stages.  pt = thread index among the copy threads.
-template <int NS>
+// of NS stages.  pt = thread index among the copy threads.  FIRST: the K/V
+// rows leave L2 first (a pass whose only reader of a chunk is this CTA).
+template <int NS, bool FIRST>
 SPEC_DEV void copy_stages(const AttnParams& p, const Chunk& ch, uint8_t* stages, int32_t* bt_s,
                           uint64_t* kv_full, uint64_t* kv_empty, int pt) {
   const int P = p.page_size;
@@ -103,6 +104,11 @@ SPEC_DEV void copy_stages(const AttnParams& p, const Chunk& ch, uint8_t* stages,
   const uint8_t* vcol = reinterpret_cast<const uint8_t*>(p.v) + (size_t)ch.kvh * 256 + c4 * 64;
   const bool pow2 = (P & (P - 1)) == 0;
   const int pshift = __ffs(P) - 1;
+  uint64_t pol;
+  if (FIRST)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
   for (int k = 0; k < ch.nst; ++k) {
     const int slot = k % NS;
     if (k >= NS && !mbar_wait(&kv_empty[slot], ((k / NS) - 1) & 1, p.err, p.wait_ns)) break;
@@ -123,12 +129,13 @@ SPEC_DEV void copy_stages(const AttnParams& p, const Chunk& ch, uint8_t* stages,
       const uint32_t drow = sbase + tok * 128;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(drow + col[u]),
-                     "l"(kcol + row + 16 * u), "r"(n)
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                         drow + col[u]),
+                     "l"(kcol + row + 16 * u), "r"(n), "l"(pol)
                      : "memory");
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
                          drow + col[u] + 2 * kHalf),
-                     "l"(vcol + row + 16 * u), "r"(n)
+                     "l"(vcol + row + 16 * u), "r"(n), "l"(pol)
                      : "memory");
       }
     }
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(one::kThreads, 1) attn_partial_tc1(const AttnP
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= kCopyWarp0) {
-    copy_stages<kStages>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
+    copy_stages<kStages, true>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, p.err, p.wait_ns);
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(two::kThreads, 1) attn_partial_tc2(const AttnP
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= kCopyWarp0) {
-    copy_stages<kStages>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
+    copy_stages<kStages, false>(p, ch, stages, bt_s, kv_full, kv_empty, threadIdx.x - 32 * kCopyWarp0);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, p.err, p.wait_ns);
