@@ -23,7 +23,7 @@
 // The normaliser, the top-k / top-p cut and the draws need at most four
 // cluster exchanges per row:
 //   1. row maximum (and argmax, greedy);
-//   2. Z, and (truncation only) a histogram of E: 16 bins per octave of E
+//   2. Z, and (truncation only) a histogram of E: 32 bins per octave of E
 //      (all E of a bin share one exponent), each holding its element count
 //      and the sum of its rounded 16-bit significands, which locates the
 //      bins the cut can fall in;
@@ -39,10 +39,17 @@
 // selection over the logit keys.  Shared-memory atomics are 32-bit only:
 // 64-bit and float atomics on shared memory are many times slower on sm_103.
 //
+// Many truncated rows at once (more cluster CTAs than twice the SMs) take the
+// streaming kernel further below instead: one 1024-thread CTA per row, one
+// sweep of the row into per-warp candidate lists, no cluster exchanges.
+//
 // Numerics: exp((l - m)/T) = 2^x with x = (l - m) * (1/(T ln 2)) carried as
 // a float pair (Knuth's TwoSum for l - m, an FMA for the product error, the
 // constant split in two floats) and 2^x_hi * (1 + x_lo ln 2) on the
-// special-function unit; p matches a float64 evaluation to a few 1e-7.
+// special-function unit; p matches a float64 evaluation to a few 1e-7.  When
+// p is not returned (FAST), 2^x is one SFU exp2 of a single FMA: the
+// decisions it feeds are compared with the oracle's, and the draws and tests
+// within 1e-5 of a threshold are the ones flagged.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -1709,19 +1716,21 @@ __global__ void __launch_bounds__(NT, 512 / NT) sampler_kernel(const SP p) {
 
 // ---------------------------------------------------------------- streaming kernel (many rows)
 // One 1024-thread CTA per target row, used for truncated sampling when many
-// rows run at once.  The row is read from global memory twice: from HBM for
-// the maximum (with one evenly spaced sample per thread), then, E recomputed
-// and the row now in L2, for Z, setting one bit per id at or above a floor
-// that the samples place so that about kSBudget ids pass.  Each warp turns
-// its bits into an id-ordered candidate list (ids and logits, shared memory);
-// the histogram, the members of the crossing bins, the kept set and the draws
-// all work on those lists.  A floor above the cut, or a list that overflows,
-// falls back to further sweeps of the row.  No cluster exchanges: every SM
-// works on its own rows.
+// rows run at once.  One evenly spaced sample per thread gives a reference
+// maximum and a candidate floor that about kSBudget ids pass; then ONE sweep
+// of the row from HBM (each warp its own contiguous id range) takes the
+// maximum, Z relative to the reference (rescaled to the maximum after it) and
+// appends every id at or above the floor, with its logit, to the warp's
+// id-ordered candidate list in shared memory.  The histogram, the members of
+// the crossing bins, the kept set and the draws all work on those lists.  A
+// floor above the cut, or a list that overflows, falls back to further
+// sweeps of the row.  No cluster exchanges: every SM works on its own rows.
+// (The two-pass variant, PRE, takes the sweep's results from a pre-pass over
+// all SMs instead.)
 constexpr int kSNT = 1024;
 constexpr int kSCap = 16384;    // list entries per row (kSCap / 32 per warp)
 constexpr int kSBudget = 10240; // candidates a row's floor aims at (sampled estimate)
-constexpr int kSListMaxV = 163840;  // rows up to this long are listed (one flag bit per id)
+constexpr int kSListMaxV = 163840;  // rows up to this long are listed; longer ones are histogrammed whole
 
 // Each warp of the row kernel owns one contiguous range of the row's ids
 // (a multiple of 32 long); the two-pass variant's pre-pass sweeps each such
